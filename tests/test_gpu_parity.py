@@ -1,0 +1,185 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Small shapes are compared element by element in full (several 128-row tiles,
+ragged tails, GQA, causal with Tq == Tk, Tq < Tk and Tq > Tk, empty rows).
+The five named workloads run at full size in the same launch configuration
+the benchmark times; the oracle checks sampled forward rows of several heads
+and one complete GQA group (all of its query heads and rows, so dK and dV are
+complete) of the backward.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.parity import assert_close, assert_L_close, errors
+from tiled_attention_05_gb300.inputs import WORKLOADS, WORKLOAD_ORDER, make_custom, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import tiled_attention_05_gb300 as lib
+
+    lib.load()
+    return lib
+
+
+def run_gpu(fa, Q, K, V, dO, causal, scale=None, backward=True):
+    dev = torch.device("cuda")
+    Qd, Kd, Vd, dOd = (t.to(dev) for t in (Q, K, V, dO))
+    O, L = fa.fa_forward(Qd, Kd, Vd, causal, scale)
+    out = {"O": O, "L": L}
+    if backward:
+        dQ, dK, dV = fa.fa_backward(Qd, Kd, Vd, O, dOd, L, causal, scale)
+        out.update(dQ=dQ, dK=dK, dV=dV)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == 0
+    return {k: v.cpu() for k, v in out.items()}
+
+
+SMALL = [
+    # B, Hq, Hkv, Tq, Tk, d, causal
+    (1, 1, 1, 256, 256, 64, False),      # the single-head workload shape
+    (2, 4, 2, 300, 333, 128, False),     # ragged q and kv tails, GQA 2:1
+    (2, 4, 2, 300, 300, 128, True),      # causal, ragged
+    (1, 4, 1, 200, 520, 64, True),       # causal Tq < Tk (bottom-right)
+    (1, 2, 2, 513, 257, 128, True),      # causal Tq > Tk: the first rows see no key
+    (1, 8, 2, 129, 17, 64, False),       # one key tile, mostly padding
+    (1, 1, 1, 1, 1, 128, False),         # one row, one key
+    (1, 2, 1, 17, 129, 128, True),
+    (3, 4, 4, 384, 384, 64, True),       # exact multiples of the tile
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s[:6])) + ("c" if s[6] else ""))
+def test_small_shapes_full_parity(fa, shape):
+    B, Hq, Hkv, Tq, Tk, d, causal = shape
+    Q, K, V, dO = make_custom(B, Hq, Hkv, Tq, Tk, d, causal, seed=sum(shape[:6]))
+    got = run_gpu(fa, Q, K, V, dO, causal)
+    O, L = oracle.forward(Q, K, V, causal)
+    dQ, dK, dV, _ = oracle.backward(Q, K, V, dO, causal)
+    assert_close("O", got["O"], O)
+    assert_L_close("L", got["L"], L)
+    assert_close("dQ", got["dQ"], dQ)
+    assert_close("dK", got["dK"], dK)
+    assert_close("dV", got["dV"], dV)
+
+
+def test_explicit_scale(fa):
+    Q, K, V, dO = make_custom(1, 2, 1, 200, 260, 128, False, seed=7)
+    got = run_gpu(fa, Q, K, V, dO, False, scale=0.05)
+    O, L = oracle.forward(Q, K, V, False, 0.05)
+    dQ, dK, dV, _ = oracle.backward(Q, K, V, dO, False, 0.05)
+    assert_close("O", got["O"], O)
+    assert_L_close("L", got["L"], L)
+    for n, ref in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+        assert_close(n, got[n], ref)
+
+
+def test_empty_key_policy(fa):
+    # Tk = 0: O = 0, L = -inf, dQ = 0
+    Q, K, V, dO = make_custom(1, 2, 1, 40, 1, 64, False, seed=3)
+    K, V = K[:, :, :0].contiguous(), V[:, :, :0].contiguous()
+    dev = torch.device("cuda")
+    Qd, dOd = Q.to(dev), dO.to(dev)
+    Kd = torch.empty(1, 1, 0, 64, dtype=torch.bfloat16, device=dev)
+    Vd = torch.empty(1, 1, 0, 64, dtype=torch.bfloat16, device=dev)
+    O, L = fa.fa_forward(Qd, Kd, Vd, False)
+    dQ, dK, dV = fa.fa_backward(Qd, Kd, Vd, O, dOd, L, False)
+    torch.cuda.synchronize()
+    assert torch.all(O == 0) and torch.all(torch.isneginf(L)) and torch.all(dQ == 0)
+
+
+def test_zero_rows_noop(fa):
+    dev = torch.device("cuda")
+    Q = torch.empty(1, 2, 0, 128, dtype=torch.bfloat16, device=dev)
+    K = torch.randn(1, 1, 50, 128, device=dev).to(torch.bfloat16)
+    V = torch.randn(1, 1, 50, 128, device=dev).to(torch.bfloat16)
+    O, L = fa.fa_forward(Q, K, V, True)
+    dQ, dK, dV = fa.fa_backward(Q, K, V, O, torch.empty_like(O), L, True)
+    torch.cuda.synchronize()
+    assert O.numel() == 0 and torch.all(dK == 0) and torch.all(dV == 0)
+
+
+def test_misaligned_pointer_rejected(fa):
+    dev = torch.device("cuda")
+    base = torch.randn(1, 1, 64 * 128 + 1, device=dev).to(torch.bfloat16)
+    Q = base.view(-1)[1:].view(1, 1, 64, 128)  # 2-byte offset
+    K = torch.randn(1, 1, 64, 128, device=dev).to(torch.bfloat16)
+    with pytest.raises(fa.FAError) as e:
+        fa.fa_forward(Q, K, K, False)
+    assert e.value.code == fa.FA_ERR_INVALID_ARG
+
+
+def test_saved_state_is_O_and_L_only(fa):
+    """The page's instrument (saved_tensors_hooks) on the autograd wrapper: the
+    backward keeps Q, K, V (the inputs) plus O and L and nothing quadratic."""
+    B, Hq, Hkv, T, d = 2, 4, 2, 1000, 128
+    dev = torch.device("cuda")
+    Q, K, V, dO = (t.to(dev) for t in make_custom(B, Hq, Hkv, T, T, d, True, seed=11))
+    Q.requires_grad_(True)
+    K.requires_grad_(True)
+    V.requires_grad_(True)
+    seen, total = set(), [0]
+
+    def pack(t):
+        key = (t.untyped_storage().data_ptr(), t.storage_offset(), tuple(t.shape), tuple(t.stride()), t.dtype)
+        if key not in seen:
+            seen.add(key)
+            total[0] += t.numel() * t.element_size()
+        return t
+
+    with torch.autograd.graph.saved_tensors_hooks(pack, lambda t: t):
+        O = fa.attention(Q, K, V, True)
+        (O.float() * dO.float()).sum().backward()
+    want = oracle.saved_bytes("keep_o_l", B, Hq, Hkv, T, T, d, d, elem_bytes=2, stat_bytes=4)
+    assert total[0] == want
+    dense = oracle.saved_bytes("dense", B, Hq, Hkv, T, T, d, d, elem_bytes=2, prob_bytes=2)
+    assert total[0] < dense / 5
+
+
+# ------------------------------------------------------------------ full-size workloads
+def sample_rows(Tq):
+    """Query rows to check: tile boundaries, the ragged end, a spread in between."""
+    rows = {0, 1, 127, 128, Tq // 2, Tq - 129, Tq - 128, Tq - 1}
+    rows |= set(range(5, Tq, max(1, Tq // 16)))
+    return sorted(r for r in rows if 0 <= r < Tq)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", WORKLOAD_ORDER)
+def test_workload_full_size(fa, name):
+    w = WORKLOADS[name]
+    Q, K, V, dO = make_inputs(w)
+    got = run_gpu(fa, Q, K, V, dO, w.causal)
+    G = w.G
+    # forward: sampled rows of the first and last head of the first and last batch
+    heads = sorted({(0, 0), (0, w.Hq - 1), (w.B - 1, w.Hq // 2), (w.B - 1, w.Hq - 1)})
+    rows = sample_rows(w.Tq)
+    for b, h in heads:
+        kvh = h // G
+        Qh, Kh, Vh = (oracle._f64(t) for t in (Q[b:b + 1, h:h + 1], K[b:b + 1, kvh:kvh + 1],
+                                                 V[b:b + 1, kvh:kvh + 1]))
+        for r in rows:
+            O, L = oracle.forward(Qh, Kh, Vh, w.causal, rows=(r, r + 1))
+            assert_close(f"O[{b},{h},{r}]", got["O"][b, h, r], O[0, 0, r])
+            assert_L_close(f"L[{b},{h},{r}]", got["L"][b, h, r:r + 1], L[0, 0, r:r + 1])
+    # backward: one complete GQA group (the last one: last batch, last kv head).
+    b, kvh = w.B - 1, w.Hkv - 1
+    hs = slice(kvh * G, (kvh + 1) * G)
+    dQ, dK, dV, _ = oracle.backward(Q[b:b + 1, hs], K[b:b + 1, kvh:kvh + 1], V[b:b + 1, kvh:kvh + 1],
+                                    dO[b:b + 1, hs], w.causal)
+    assert_close("dQ(group)", got["dQ"][b:b + 1, hs], dQ)
+    assert_close("dK(group)", got["dK"][b:b + 1, kvh:kvh + 1], dK)
+    assert_close("dV(group)", got["dV"][b:b + 1, kvh:kvh + 1], dV)
+    # the whole output is finite
+    for n in ("O", "L", "dQ", "dK", "dV"):
+        assert torch.isfinite(got[n].float()).all(), n

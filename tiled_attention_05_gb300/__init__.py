@@ -1,0 +1,198 @@
+"""Python binding of the GB300 tiled exact attention library (include/fa.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libfa_gb300.so``.  There is no CPU or PyTorch fallback -- if the
+library cannot be loaded, every entry point raises.
+
+Entry points mirror the C ABI:
+    fa_forward(Q, K, V, causal, scale=None)            -> (O, L)
+    fa_backward(Q, K, V, O, dO, L, causal, scale=None)  -> (dQ, dK, dV)
+    fa_backward_workspace_bytes(...), fa_status_string(code), fa_last_device_status()
+plus ``FlashAttention`` (a torch.autograd.Function that keeps only Q, K, V, O
+and L for the backward pass) and ``attention`` (its functional form).
+
+Tensors are CUDA bf16, contiguous, [B, H, T, d]; L is fp32 [B, Hq, Tq].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+
+EXPORTED_SYMBOLS = ("fa_forward", "fa_backward", "fa_backward_stages", "fa_backward_workspace_bytes",
+                    "fa_status_string", "fa_last_device_status", "fa_last_launch_count")
+FA_BWD_PRE, FA_BWD_MAIN, FA_BWD_CAST, FA_BWD_ALL = 1, 2, 4, 7
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+
+
+class FaDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("Tq", ctypes.c_int),
+                ("Tk", ctypes.c_int), ("d", ctypes.c_int), ("dv", ctypes.c_int), ("causal", ctypes.c_int),
+                ("scale", ctypes.c_float)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the shared library; raises if that fails."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or _build.build()
+            if not os.path.exists(p):
+                raise RuntimeError(f"CUDA attention library missing: {p}")
+            lib = ctypes.CDLL(p)
+            vp, dp = ctypes.c_void_p, ctypes.POINTER(FaDims)
+            lib.fa_forward.argtypes = [dp, vp, vp, vp, vp, vp, vp]
+            lib.fa_forward.restype = ctypes.c_int
+            lib.fa_backward.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+            lib.fa_backward.restype = ctypes.c_int
+            lib.fa_backward_stages.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
+                                               ctypes.c_int, vp]
+            lib.fa_backward_stages.restype = ctypes.c_int
+            lib.fa_backward_workspace_bytes.argtypes = [dp]
+            lib.fa_backward_workspace_bytes.restype = ctypes.c_size_t
+            lib.fa_status_string.argtypes = [ctypes.c_int]
+            lib.fa_status_string.restype = ctypes.c_char_p
+            lib.fa_last_device_status.argtypes = [vp]
+            lib.fa_last_device_status.restype = ctypes.c_int
+            lib.fa_last_launch_count.argtypes = []
+            lib.fa_last_launch_count.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().fa_status_string(int(code)).decode()
+
+
+fa_status_string = status_string
+
+
+def make_dims(B, Hq, Hkv, Tq, Tk, d, dv, causal, scale) -> FaDims:
+    return FaDims(int(B), int(Hq), int(Hkv), int(Tq), int(Tk), int(d), int(dv), int(bool(causal)),
+                  float(scale) if scale is not None else 0.0)
+
+
+def _dims_of(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, causal, scale) -> FaDims:
+    if Q.dim() != 4 or K.dim() != 4 or V.dim() != 4:
+        raise ValueError("Q, K, V must be [B, H, T, d]")
+    B, Hq, Tq, d = Q.shape
+    Bk, Hkv, Tk, dk = K.shape
+    Bv, Hv, Tv, dv = V.shape
+    if not (B == Bk == Bv and Hkv == Hv and Tk == Tv and d == dk):
+        raise ValueError(f"inconsistent shapes Q{tuple(Q.shape)} K{tuple(K.shape)} V{tuple(V.shape)}")
+    return make_dims(B, Hq, Hkv, Tq, Tk, d, dv, causal, scale)
+
+
+def _check(t: torch.Tensor, name: str, dtype=torch.bfloat16):
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def _stream_ptr(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _raise(code: int, where: str):
+    if code != FA_OK:
+        raise FAError(code, where)
+
+
+def fa_backward_workspace_bytes(dims: FaDims) -> int:
+    return int(load().fa_backward_workspace_bytes(ctypes.byref(dims)))
+
+
+def fa_forward(Q, K, V, causal: bool, scale: float | None = None, O=None, L=None, stream=None):
+    """O, L = attention forward.  Optional preallocated O / L are written in place."""
+    lib = load()
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _check(t, n)
+    dims = _dims_of(Q, K, V, causal, scale)
+    if O is None:
+        O = torch.empty(dims.B, dims.Hq, dims.Tq, dims.dv, dtype=torch.bfloat16, device=Q.device)
+    if L is None:
+        L = torch.empty(dims.B, dims.Hq, dims.Tq, dtype=torch.float32, device=Q.device)
+    _check(O, "O")
+    _check(L, "L", torch.float32)
+    code = lib.fa_forward(ctypes.byref(dims), Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                          L.data_ptr(), _stream_ptr(stream))
+    _raise(code, "fa_forward")
+    return O, L
+
+
+def fa_backward(Q, K, V, O, dO, L, causal: bool, scale: float | None = None, dQ=None, dK=None, dV=None,
+                workspace=None, stream=None, stages: int = FA_BWD_ALL):
+    """dQ, dK, dV = attention backward from the saved O and L.
+
+    ``stages`` selects which of the three backward kernels to launch (see
+    fa_backward_stages in include/fa.h); the default runs all of them.
+    """
+    lib = load()
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (dO, "dO")):
+        _check(t, n)
+    _check(L, "L", torch.float32)
+    dims = _dims_of(Q, K, V, causal, scale)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    for t, n in ((dQ, "dQ"), (dK, "dK"), (dV, "dV")):
+        _check(t, n)
+    need = fa_backward_workspace_bytes(dims)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=Q.device)
+    args = (ctypes.byref(dims), Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), dO.data_ptr(),
+            L.data_ptr(), dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), workspace.data_ptr(), workspace.numel())
+    if stages == FA_BWD_ALL:
+        code = lib.fa_backward(*args, _stream_ptr(stream))
+    else:
+        code = lib.fa_backward_stages(*args, int(stages), _stream_ptr(stream))
+    _raise(code, "fa_backward")
+    return dQ, dK, dV
+
+
+def fa_last_device_status(stream=None) -> int:
+    return int(load().fa_last_device_status(_stream_ptr(stream)))
+
+
+def last_launch_count() -> int:
+    return int(load().fa_last_launch_count())
+
+
+class FlashAttention(torch.autograd.Function):
+    """Autograd wrapper: saves Q, K, V (inputs) plus O and L -- nothing quadratic."""
+
+    @staticmethod
+    def forward(ctx, Q, K, V, causal=False, scale=None):
+        O, L = fa_forward(Q, K, V, causal, scale)
+        ctx.save_for_backward(Q, K, V, O, L)
+        ctx.causal, ctx.scale = causal, scale
+        return O
+
+    @staticmethod
+    def backward(ctx, dO):
+        Q, K, V, O, L = ctx.saved_tensors
+        dQ, dK, dV = fa_backward(Q, K, V, O, dO.contiguous(), L, ctx.causal, ctx.scale)
+        return dQ, dK, dV, None, None
+
+
+def attention(Q, K, V, causal=False, scale=None):
+    return FlashAttention.apply(Q, K, V, causal, scale)

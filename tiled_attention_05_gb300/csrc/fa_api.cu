@@ -1,0 +1,192 @@
+// C ABI of the attention library: argument validation, TMA descriptor
+// encoding, the device status word and the workspace query.  The kernels and
+// their launchers live in fa_fwd.cu and fa_bwd.cu.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace {
+
+__device__ int g_fa_status;  // 0, or a kernel's DEV_* code after a bounded wait gave up
+
+thread_local int t_last_launches = 0;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices];
+std::mutex g_status_mu;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates dims; on success fills *pr.  Null data pointers are only an error
+// when the tensor they point to is non-empty.
+fa_status check_dims(const fa_dims* dims, fa::Problem* pr) {
+  if (!dims) return FA_ERR_INVALID_ARG;
+  const fa_dims& z = *dims;
+  if (z.B < 0 || z.Hq < 0 || z.Hkv < 0 || z.Tq < 0 || z.Tk < 0 || z.d < 1 || z.dv < 1) return FA_ERR_INVALID_ARG;
+  if (z.causal != 0 && z.causal != 1) return FA_ERR_INVALID_ARG;
+  if (z.Hq > 0 && (z.Hkv < 1 || z.Hq % z.Hkv != 0)) return FA_ERR_INVALID_ARG;
+  if (!(z.scale == z.scale) || std::isinf(z.scale)) return FA_ERR_INVALID_ARG;
+  if (z.dv != z.d || (z.d != 64 && z.d != 128)) return FA_ERR_UNSUPPORTED;
+  // TMA coordinates and grid dimensions are 32-bit; keep every index in range.
+  if ((long long)z.B * z.Hq > 0x7fffffffLL || (long long)z.B * z.Hkv > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (z.Tq > (1 << 30) || z.Tk > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  pr->B = z.B;
+  pr->Hq = z.Hq;
+  pr->Hkv = z.Hkv;
+  pr->Tq = z.Tq;
+  pr->Tk = z.Tk;
+  pr->d = z.d;
+  pr->causal = z.causal;
+  pr->scale = z.scale > 0.f ? z.scale : 1.0f / std::sqrt((float)z.d);
+  return FA_OK;
+}
+
+fa_status check_ptr(const void* p, long long elems) {
+  if (elems == 0) return FA_OK;
+  if (!p || !aligned16(p)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+}  // namespace
+
+namespace fa {
+
+bool encode_rows_bf16(CUtensorMap* map, const void* base, int inner, int rows, long long outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * 2 * (cuuint64_t)rows};
+  cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int* device_status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_forward(const fa_dims* dims, const void* Q, const void* K, const void* V, void* O, float* L,
+                     void* stream) {
+  t_last_launches = 0;
+  fa::Problem pr;
+  fa_status s = check_dims(dims, &pr);
+  if (s != FA_OK) return s;
+  const long long nq = (long long)pr.B * pr.Hq * pr.Tq * pr.d;
+  const long long nk = (long long)pr.B * pr.Hkv * pr.Tk * pr.d;
+  if ((s = check_ptr(Q, nq)) || (s = check_ptr(K, nk)) || (s = check_ptr(V, nk)) || (s = check_ptr(O, nq)) ||
+      (s = check_ptr(L, (long long)pr.B * pr.Hq * pr.Tq)))
+    return s;
+  if (nq == 0) return FA_OK;
+  if (!fa::device_status_word()) return FA_ERR_CUDA;
+  int launches = 0;
+  cudaError_t e = fa::launch_forward(pr, Q, K, V, O, L, static_cast<cudaStream_t>(stream), &launches);
+  t_last_launches = launches;
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_backward_workspace_bytes(const fa_dims* dims) {
+  fa::Problem pr;
+  if (check_dims(dims, &pr) != FA_OK) return 0;
+  return fa::backward_workspace_layout(pr).total;
+}
+
+fa_status fa_backward_stages(const fa_dims* dims, const void* Q, const void* K, const void* V, const void* O,
+                             const void* dO, const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                             size_t workspace_bytes, int stages, void* stream) {
+  t_last_launches = 0;
+  fa::Problem pr;
+  fa_status s = check_dims(dims, &pr);
+  if (s != FA_OK) return s;
+  if (stages < 0 || stages > FA_BWD_ALL) return FA_ERR_INVALID_ARG;
+  const long long nq = (long long)pr.B * pr.Hq * pr.Tq * pr.d;
+  const long long nk = (long long)pr.B * pr.Hkv * pr.Tk * pr.d;
+  if ((s = check_ptr(Q, nq)) || (s = check_ptr(K, nk)) || (s = check_ptr(V, nk)) || (s = check_ptr(O, nq)) ||
+      (s = check_ptr(dO, nq)) || (s = check_ptr(L, (long long)pr.B * pr.Hq * pr.Tq)) || (s = check_ptr(dQ, nq)) ||
+      (s = check_ptr(dK, nk)) || (s = check_ptr(dV, nk)))
+    return s;
+  if ((nq == 0 && nk == 0) || stages == 0) return FA_OK;
+  const size_t need = fa::backward_workspace_layout(pr).total;
+  if (nq > 0 && nk > 0) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+      return FA_ERR_INVALID_ARG;
+  }
+  if (!fa::device_status_word()) return FA_ERR_CUDA;
+  int launches = 0;
+  cudaError_t e = fa::launch_backward(pr, Q, K, V, O, dO, L, dQ, dK, dV, workspace, stages,
+                                      static_cast<cudaStream_t>(stream), &launches);
+  t_last_launches = launches;
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_backward(const fa_dims* dims, const void* Q, const void* K, const void* V, const void* O,
+                      const void* dO, const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  return fa_backward_stages(dims, Q, K, V, O, dO, L, dQ, dK, dV, workspace, workspace_bytes, FA_BWD_ALL, stream);
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK:
+      return "ok";
+    case FA_ERR_INVALID_ARG:
+      return "invalid argument (null or misaligned pointer, negative size, Hq not a multiple of Hkv, "
+             "bad causal flag or scale, or workspace too small)";
+    case FA_ERR_UNSUPPORTED:
+      return "unsupported shape (d must equal dv and be 64 or 128)";
+    case FA_ERR_CUDA:
+      return "CUDA error while encoding tensor maps or launching kernels";
+    case FA_ERR_TIMEOUT:
+      return "a kernel gave up waiting on an on-chip barrier; outputs are undefined";
+  }
+  return "unknown status";
+}
+
+fa_status fa_last_device_status(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+  int* w = fa::device_status_word();
+  if (!w) return FA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyAsync(&v, w, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemsetAsync(w, 0, sizeof(int), st) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+  return v == 0 ? FA_OK : FA_ERR_TIMEOUT;
+}
+
+int fa_last_launch_count(void) { return t_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,579 @@
+// Backward pass of tiled exact attention on sm_103a.
+//
+// Method ("What Ordinary Autograd Saves", section "Why this is
+// FlashAttention's second idea"; "Backward Pass Implementation", section "The
+// Recomputation Strategy"): only O and the row statistic L survive the
+// forward; every score/probability tile is rebuilt on chip from Q, K and L.
+// With D_i = rowsum(dO_i * O_i):
+//     P = exp(scale * Q K^T - L),  dP = dO V^T,  dS = P * (dP - D),
+//     dV += P^T dO,  dK += dS^T Q * scale,  dQ += dS K * scale.
+//
+// Three kernels:
+//   fa_bwd_pre   D = rowsum(dO * O), L in log2 units (+inf on padding rows so
+//                that their probabilities vanish), zero the fp32 dQ
+//                accumulator.  HBM-bound, one warp per row.
+//   fa_bwd_main  one CTA per (batch, kv head, 128-key tile): K and V stay in
+//                shared memory; the CTA walks the G query heads of its group
+//                and their 128-row query tiles, keeping dK and dV in TMEM for
+//                the whole walk and adding each tile's dQ into the fp32
+//                accumulator in global memory.
+//   fa_dq_cast   dQ = bf16(scale * accumulator).  HBM-bound.
+//
+// fa_bwd_main roles (320 threads):
+//   warp 0      TMA: K, V once; then Q_t, dO_t (+ the tile's L and D slices by
+//               1-D bulk copy) through a 2-deep ring.
+//   warp 1      tcgen05 issuer, per tile t:
+//                 S^T  = K Q_t^T        -> TMEM [0,128)      (kv rows = lanes)
+//                 dP^T = V dO_t^T       -> TMEM [128,256)
+//                 dV  += P^T dO_t       A = P^T from TMEM (bf16, written over S^T)
+//                 dK  += dS^T Q_t       A = dS^T from shared memory (K-major)
+//                 dQ_t = dS K           -> TMEM [128,128+d)  A = the same dS bytes
+//                                        read MN-major; B = K read MN-major
+//   warps 2..9  two elementwise warpgroups (thread = key row = TMEM lane; group
+//               w owns query columns [64w, 64w+64)): P = exp2(S*scale*log2e - L2),
+//               masks; dS = P * (dP - D) -> shared memory; then drain their
+//               half of dQ_t from TMEM with vector fp32 reductions to global.
+//               Epilogue: dV and dK*scale -> bf16 -> TMA store.
+// TMEM columns: S^T/P [0,128), dP^T/dQ [128,256), dV [256,256+d), dK [256+d, 256+2d).
+#include <cstdint>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+using namespace fa_ptx;
+
+namespace {
+
+constexpr int BM = fa::kTile;  // query rows per tile
+constexpr int BN = fa::kTile;  // keys per CTA
+constexpr int kThreads = 320;
+
+template <int HD>
+struct BwdCfg {
+  static constexpr int TILE = 128 * HD * 2;  // one Q, dO, K or V tile (bf16)
+  static constexpr int DS_BYTES = BN * BM * 2;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_Q = OFF_V + TILE;    // [2]
+  static constexpr int OFF_DO = OFF_Q + 2 * TILE;  // [2]
+  static constexpr int OFF_DS = OFF_DO + 2 * TILE;
+  static constexpr int OFF_LSE = OFF_DS + DS_BYTES;    // [2][128] fp32
+  static constexpr int OFF_DELTA = OFF_LSE + 2 * 512;  // [2][128] fp32
+  static constexpr int OFF_BAR = OFF_DELTA + 2 * 512;
+  static constexpr int NBAR = 16;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct BwdParams {
+  float* dq_acc;
+  const float* lse2;
+  const float* delta;
+  int* status;
+  int Hq, Hkv, G, Tq, Tk, causal_off, q_tiles;
+  long long Tq_pad;
+  float scale_log2, scale;
+};
+
+template <int HD, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                const BwdParams p) {
+  using C = BwdCfg<HD>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* qdo_full = bars + 1;   // [2]
+  uint64_t* qdo_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;
+  uint64_t* dp_full = bars + 6;
+  uint64_t* p_ready = bars + 7;
+  uint64_t* ds_ready = bars + 8;
+  uint64_t* tS_free = bars + 9;
+  uint64_t* dq_full = bars + 10;
+  uint64_t* dq_empty = bars + 11;
+  uint64_t* acc_done = bars + 12;
+  uint64_t* drain = bars + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bkv = blockIdx.x;
+  const int b = bkv / p.Hkv, hk = bkv - b * p.Hkv;
+  const int n = blockIdx.y;  // key tile; causal: low tiles see the most query rows, run first
+  const int k0 = n * BN;
+
+  int m_begin = 0;
+  if (CAUSAL) {
+    const int first_row = k0 - p.causal_off;  // first query row that sees key k0
+    m_begin = first_row <= 0 ? 0 : min(p.q_tiles, first_row / BM);
+  }
+  const int n_m = p.q_tiles - m_begin;
+  const int T = p.G * n_m;  // tiles this CTA walks
+
+  if (threadIdx.x == 0) {
+    *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&qdo_full[s], 1);
+      mbar_init(&qdo_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_ready, 256);
+    mbar_init(ds_ready, 256);
+    mbar_init(tS_free, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 256);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool run = (*abort_flag == 0) && T > 0;
+  const uint32_t T_S = tmem, T_DP = tmem + 128, T_DV = tmem + 256, T_DK = tmem + 256 + HD;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && run) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmdO);
+      mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+#pragma unroll
+      for (int cb = 0; cb < HD / 64; ++cb) {
+        tma_load_3d(smem + C::OFF_K + cb * BN * 128, &tmK, kv_full, cb * 64, k0, bkv);
+        tma_load_3d(smem + C::OFF_V + cb * BN * 128, &tmV, kv_full, cb * 64, k0, bkv);
+      }
+      int last[2] = {-1, -1};
+      for (int t = 0; t < T; ++t) {
+        const int st = t & 1, u = t >> 1;
+        const int g = t / n_m, m = m_begin + (t - g * n_m);
+        const int bh = b * p.Hq + hk * p.G + g;
+        if (!mbar_wait(&qdo_empty[st], (u & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&qdo_full[st], 2 * C::TILE + 1024);
+#pragma unroll
+        for (int cb = 0; cb < HD / 64; ++cb) {
+          tma_load_3d(smem + C::OFF_Q + st * C::TILE + cb * BM * 128, &tmQ, &qdo_full[st], cb * 64, m * BM, bh);
+          tma_load_3d(smem + C::OFF_DO + st * C::TILE + cb * BM * 128, &tmdO, &qdo_full[st], cb * 64, m * BM, bh);
+        }
+        const long long row0 = (long long)bh * p.Tq_pad + (long long)m * BM;
+        bulk_load(smem + C::OFF_LSE + st * 512, p.lse2 + row0, 512, &qdo_full[st]);
+        bulk_load(smem + C::OFF_DELTA + st * 512, p.delta + row0, 512, &qdo_full[st]);
+        last[st] = u;
+      }
+      mbar_wait_bounded(kv_full, 0);
+      for (int st = 0; st < 2; ++st)
+        if (last[st] >= 0) mbar_wait_bounded(&qdo_full[st], last[st] & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && run) {
+      constexpr uint32_t id_sdp = idesc_bf16(BN, BM, 0, 0);  // S^T, dP^T: M = keys, N = queries
+      constexpr uint32_t id_kv = idesc_bf16(BN, HD, 0, 1);   // dV, dK: M = keys, N = d, B MN-major
+      constexpr uint32_t id_q = idesc_bf16(BM, HD, 1, 1);    // dQ: M = queries (A MN-major), N = d
+      const uint32_t k_base = smem_u32(smem + C::OFF_K), v_base = smem_u32(smem + C::OFF_V);
+      const uint32_t ds_base = smem_u32(smem + C::OFF_DS);
+      bool ok = mbar_wait(kv_full, 0, abort_flag);
+      for (int t = 0; ok && t < T; ++t) {
+        const int st = t & 1, u = t >> 1;
+        const uint32_t q_base = smem_u32(smem + C::OFF_Q + st * C::TILE);
+        const uint32_t do_base = smem_u32(smem + C::OFF_DO + st * C::TILE);
+        if (!mbar_wait(&qdo_full[st], u & 1, abort_flag)) { ok = false; break; }
+        if (t > 0 && !mbar_wait(tS_free, (t - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          mma_ss(T_S, desc_kmajor(k_base + (k >> 2) * (BN * 128) + (k & 3) * 32),
+                 desc_kmajor(q_base + (k >> 2) * (BM * 128) + (k & 3) * 32), id_sdp, k > 0 ? 1u : 0u);
+        mma_commit(s_full);
+        if (t > 0 && !mbar_wait(dq_empty, (t - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          mma_ss(T_DP, desc_kmajor(v_base + (k >> 2) * (BN * 128) + (k & 3) * 32),
+                 desc_kmajor(do_base + (k >> 2) * (BM * 128) + (k & 3) * 32), id_sdp, k > 0 ? 1u : 0u);
+        mma_commit(dp_full);
+        if (!mbar_wait(p_ready, t & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        // P^T lives in TMEM as packed bf16: query columns [0,64) at TMEM columns
+        // [0,32), query columns [64,128) at [64,96) (each warpgroup overwrote its
+        // own half of S^T).
+#pragma unroll
+        for (int k = 0; k < BM / 16; ++k)
+          mma_ts(T_DV, T_S + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(do_base + k * 2048, BM * 128), id_kv,
+                 (t > 0 || k > 0) ? 1u : 0u);
+        mma_commit(tS_free);
+        if (!mbar_wait(ds_ready, t & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BM / 16; ++k)
+          mma_ss(T_DK, desc_kmajor(ds_base + (k >> 2) * (BN * 128) + (k & 3) * 32),
+                 desc_mnmajor(q_base + k * 2048, BM * 128), id_kv, (t > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&qdo_empty[st]);
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          mma_ss(T_DP, desc_mnmajor(ds_base + k * 2048, BN * 128), desc_mnmajor(k_base + k * 2048, BN * 128), id_q,
+                 k > 0 ? 1u : 0u);
+        mma_commit(dq_full);
+      }
+      mma_commit(acc_done);
+      mma_commit(drain);
+      mbar_wait_bounded(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise warpgroups
+    const int wg = (warp - 2) >> 2;  // 0 or 1
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // TMEM lane: key row for S^T/dP^T/dV/dK, query row for dQ
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const int key = k0 + r;
+    const bool key_valid = key < p.Tk;
+    const float sl2 = p.scale_log2;
+    bool ok = run;
+    for (int t = 0; ok && t < T; ++t) {
+      const int st = t & 1, u = t >> 1;
+      const int g = t / n_m, m = m_begin + (t - g * n_m);
+      const int bh = b * p.Hq + hk * p.G + g;
+      const int q0 = m * BM;
+      const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE + st * 512);
+      const float* del_s = reinterpret_cast<const float*>(smem + C::OFF_DELTA + st * 512);
+      if (!mbar_wait(&qdo_full[st], u & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(s_full, t & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      // ---- P = exp2(S * scale * log2e - L2), masked
+      uint32_t sr[64];
+      tmem_ld32(T_S + lane_base + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(T_S + lane_base + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_wait_ld();
+      const bool need_mask = !key_valid || (CAUSAL && k0 + BN - 1 > q0 + p.causal_off);
+      // key row `key` is visible to query q0 + c iff key <= q0 + c + off
+      const int vis_from = key_valid ? (CAUSAL ? key - p.causal_off - q0 : -0x40000000) : 0x40000000;
+      float pr[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const int qc = wg * 64 + c;
+        float v = ex2(fmaf(__uint_as_float(sr[c]), sl2, -lse_s[qc]));
+        if (need_mask && qc < vis_from) v = 0.f;
+        pr[c] = v;
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+      tmem_st32(T_S + lane_base + wg * 64, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+      // ---- dS = P * (dP - D) -> shared memory (row = key, 128B-swizzled, query-contiguous)
+      if (!mbar_wait(dp_full, t & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t dr[64];
+      tmem_ld32(T_DP + lane_base + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+      tmem_ld32(T_DP + lane_base + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      tmem_wait_ld();
+      uint8_t* ds_blk = smem + C::OFF_DS + wg * (BN * 128);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = cc * 8 + 2 * e;
+          const float d0 = pr[c] * (__uint_as_float(dr[c]) - del_s[wg * 64 + c]);
+          const float d1 = pr[c + 1] * (__uint_as_float(dr[c + 1]) - del_s[wg * 64 + c + 1]);
+          w[e] = pack_bf16x2(d0, d1);
+        }
+        st_shared_v4(smem_u32(ds_blk + sw128_offset(r, cc)), w[0], w[1], w[2], w[3]);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_ready);
+      // ---- drain this warpgroup's half of dQ_t (TMEM lane = query row) into the fp32 accumulator
+      if (!mbar_wait(dq_full, t & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      constexpr int HALF = HD / 2;
+      uint32_t qr[HALF];
+#pragma unroll
+      for (int c = 0; c < HALF / 32; ++c)
+        tmem_ld32(T_DP + lane_base + wg * HALF + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&qr[c * 32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      float* dst = p.dq_acc + ((long long)bh * p.Tq_pad + q0 + r) * HD + wg * HALF;
+#pragma unroll
+      for (int c = 0; c < HALF; c += 4)
+        red_add_v4(dst + c, __uint_as_float(qr[c]), __uint_as_float(qr[c + 1]), __uint_as_float(qr[c + 2]),
+                   __uint_as_float(qr[c + 3]));
+    }
+    // ---- epilogue: dV, dK * scale -> bf16 -> shared (the Q ring, idle now) -> TMA store
+    if (ok && T > 0) {
+      if (!mbar_wait(acc_done, 0, abort_flag)) ok = false;
+      tc_fence_after();
+    }
+    const bool mine = (T == 0 || ok) && *abort_flag == 0;
+    if (named_bar_and(1, 256, mine)) {
+      constexpr int HALF = HD / 2;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
+        uint8_t* stage = smem + C::OFF_Q + which * C::TILE;
+        const float mul = which ? p.scale : 1.f;
+        const uint32_t src = (which ? T_DK : T_DV) + lane_base + wg * HALF;
+#pragma unroll
+        for (int c = 0; c < HALF / 32; ++c) {
+          uint32_t v[32];
+          if (T > 0) {
+            tmem_ld32(src + c * 32, v);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+          }
+          const int col0 = wg * HALF + c * 32;  // first d column of this chunk
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(v[8 * q + 2 * e]) * mul, __uint_as_float(v[8 * q + 2 * e + 1]) * mul);
+            const int col = col0 + 8 * q;
+            st_shared_v4(smem_u32(stage + (col >> 6) * (BN * 128) + sw128_offset(r, (col & 63) >> 3)), w[0], w[1],
+                         w[2], w[3]);
+          }
+        }
+      }
+      fence_async_smem();
+      named_bar_sync(2, 256);
+      if (warp == 2 && lane == 0) {
+        prefetch_tmap(&tmdV);
+        prefetch_tmap(&tmdK);
+#pragma unroll
+        for (int cb = 0; cb < HD / 64; ++cb) {
+          tma_store_3d(&tmdV, smem + C::OFF_Q + cb * BN * 128, cb * 64, k0, bkv);
+          tma_store_3d(&tmdK, smem + C::OFF_Q + C::TILE + cb * BN * 128, cb * 64, k0, bkv);
+        }
+        bulk_commit();
+        bulk_wait0();
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicExch(p.status, DEV_TIMEOUT);
+}
+
+// D = rowsum(dO * O) and L2 = L * log2(e) per padded query row (padding rows:
+// D = 0, L2 = +inf); zeroes the row of the fp32 dQ accumulator.
+template <int HD>
+__global__ void __launch_bounds__(256) fa_bwd_pre(const uint16_t* __restrict__ O, const uint16_t* __restrict__ dO,
+                                                  const float* __restrict__ L, float* __restrict__ lse2,
+                                                  float* __restrict__ delta, float* __restrict__ dq_acc,
+                                                  long long rows_pad, int Tq, long long Tq_pad) {
+  constexpr int PER = HD / 32;  // elements per lane
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows_pad;
+       row += warps) {
+    const long long bh = row / Tq_pad;
+    const long long q = row - bh * Tq_pad;
+    float dot = 0.f;
+    if (q < Tq) {
+      const long long src = (bh * Tq + q) * HD + lane * PER;
+      if (PER == 4) {
+        const uint2 a = *reinterpret_cast<const uint2*>(O + src);
+        const uint2 g = *reinterpret_cast<const uint2*>(dO + src);
+        const uint32_t aw[2] = {a.x, a.y}, gw[2] = {g.x, g.y};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          dot += __uint_as_float(aw[e] << 16) * __uint_as_float(gw[e] << 16);
+          dot += __uint_as_float(aw[e] & 0xffff0000u) * __uint_as_float(gw[e] & 0xffff0000u);
+        }
+      } else {
+        const uint32_t a = *reinterpret_cast<const uint32_t*>(O + src);
+        const uint32_t g = *reinterpret_cast<const uint32_t*>(dO + src);
+        dot += __uint_as_float(a << 16) * __uint_as_float(g << 16);
+        dot += __uint_as_float(a & 0xffff0000u) * __uint_as_float(g & 0xffff0000u);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    if (lane == 0) {
+      delta[row] = dot;
+      lse2[row] = q < Tq ? L[bh * Tq + q] * 1.4426950408889634f : __int_as_float(0x7f800000);
+    }
+    float* acc = dq_acc + row * HD + lane * PER;
+    if (PER == 4)
+      *reinterpret_cast<float4*>(acc) = make_float4(0.f, 0.f, 0.f, 0.f);
+    else
+      *reinterpret_cast<float2*>(acc) = make_float2(0.f, 0.f);
+  }
+}
+
+// dQ = bf16(scale * accumulator), 8 elements per thread.
+template <int HD>
+__global__ void __launch_bounds__(256) fa_dq_cast(const float* __restrict__ dq_acc, uint16_t* __restrict__ dQ,
+                                                  long long n_vec, int Tq, long long Tq_pad, float scale) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < n_vec; v += stride) {
+    const long long e = v * 8;
+    const long long row = e / HD;
+    const int col = (int)(e - row * HD);
+    const long long bh = row / Tq;
+    const long long q = row - bh * Tq;
+    const float* src = dq_acc + (bh * Tq_pad + q) * HD + col;
+    const float4 a = *reinterpret_cast<const float4*>(src);
+    const float4 c = *reinterpret_cast<const float4*>(src + 4);
+    uint4 o;
+    o.x = pack_bf16x2(a.x * scale, a.y * scale);
+    o.y = pack_bf16x2(a.z * scale, a.w * scale);
+    o.z = pack_bf16x2(c.x * scale, c.y * scale);
+    o.w = pack_bf16x2(c.z * scale, c.w * scale);
+    *reinterpret_cast<uint4*>(dQ + e) = o;
+  }
+}
+
+__global__ void fa_zero_words(uint32_t* p, size_t n) {
+  for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n; t += (size_t)gridDim.x * blockDim.x) p[t] = 0u;
+}
+
+template <int HD, bool CAUSAL>
+cudaError_t launch_main_t(const fa::Problem& pr, const CUtensorMap* maps, const BwdParams& bp, cudaStream_t stream) {
+  using C = BwdCfg<HD>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(fa_bwd_main<HD, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(pr.B * pr.Hkv, pr.kv_tiles());
+  fa_bwd_main<HD, CAUSAL><<<grid, kThreads, C::SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+                                                               bp);
+  return cudaGetLastError();
+}
+
+inline int grid_for(long long work, int per_block) {
+  long long g = (work + per_block - 1) / per_block;
+  if (g > 152LL * 32) g = 152LL * 32;
+  return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+namespace fa {
+
+BwdWorkspace backward_workspace_layout(const Problem& p) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t rows = (size_t)p.B * p.Hq * (size_t)p.Tq_pad();
+  BwdWorkspace w;
+  w.dq_acc = 0;
+  w.lse2 = up(w.dq_acc + rows * p.d * sizeof(float));
+  w.delta = up(w.lse2 + rows * sizeof(float));
+  w.total = up(w.delta + rows * sizeof(float));
+  return w;
+}
+
+cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, const void* V, const void* O,
+                            const void* dO, const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                            int stages, cudaStream_t stream, int* launches) {
+  const long long q_rows = (long long)pr.B * pr.Hq * pr.Tq;
+  const long long k_rows = (long long)pr.B * pr.Hkv * pr.Tk;
+  if (q_rows == 0 && k_rows == 0) return cudaSuccess;
+  if (q_rows == 0 || pr.Tk == 0) {
+    if (!(stages & FA_BWD_MAIN)) return cudaSuccess;
+    // No query rows: dK = dV = 0.  No keys: dQ = 0.
+    if (k_rows) {
+      fa_zero_words<<<grid_for(k_rows * pr.d / 2, 256), 256, 0, stream>>>(static_cast<uint32_t*>(dK),
+                                                                         (size_t)k_rows * pr.d / 2);
+      fa_zero_words<<<grid_for(k_rows * pr.d / 2, 256), 256, 0, stream>>>(static_cast<uint32_t*>(dV),
+                                                                         (size_t)k_rows * pr.d / 2);
+      *launches += 2;
+    }
+    if (q_rows) {
+      fa_zero_words<<<grid_for(q_rows * pr.d / 2, 256), 256, 0, stream>>>(static_cast<uint32_t*>(dQ),
+                                                                         (size_t)q_rows * pr.d / 2);
+      *launches += 1;
+    }
+    return cudaGetLastError();
+  }
+  const BwdWorkspace w = backward_workspace_layout(pr);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  float* delta = reinterpret_cast<float*>(ws + w.delta);
+  const long long rows_pad = (long long)pr.B * pr.Hq * pr.Tq_pad();
+
+  cudaError_t e = cudaSuccess;
+  // 1. preprocess
+  if (stages & FA_BWD_PRE) {
+  if (pr.d == 64)
+    fa_bwd_pre<64><<<grid_for(rows_pad, 8), 256, 0, stream>>>(static_cast<const uint16_t*>(O),
+                                                              static_cast<const uint16_t*>(dO), L, lse2, delta,
+                                                              dq_acc, rows_pad, pr.Tq, pr.Tq_pad());
+  else
+    fa_bwd_pre<128><<<grid_for(rows_pad, 8), 256, 0, stream>>>(static_cast<const uint16_t*>(O),
+                                                               static_cast<const uint16_t*>(dO), L, lse2, delta,
+                                                               dq_acc, rows_pad, pr.Tq, pr.Tq_pad());
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ++*launches;
+  }
+
+  // 2. main
+  if (stages & FA_BWD_MAIN) {
+  CUtensorMap maps[6];
+  if (!encode_rows_bf16(&maps[0], Q, pr.d, pr.Tq, (long long)pr.B * pr.Hq) ||
+      !encode_rows_bf16(&maps[1], K, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
+      !encode_rows_bf16(&maps[2], V, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
+      !encode_rows_bf16(&maps[3], dO, pr.d, pr.Tq, (long long)pr.B * pr.Hq) ||
+      !encode_rows_bf16(&maps[4], dK, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
+      !encode_rows_bf16(&maps[5], dV, pr.d, pr.Tk, (long long)pr.B * pr.Hkv))
+    return cudaErrorInvalidValue;
+  BwdParams bp;
+  bp.dq_acc = dq_acc;
+  bp.lse2 = lse2;
+  bp.delta = delta;
+  bp.status = device_status_word();
+  bp.Hq = pr.Hq;
+  bp.Hkv = pr.Hkv;
+  bp.G = pr.G();
+  bp.Tq = pr.Tq;
+  bp.Tk = pr.Tk;
+  bp.causal_off = pr.Tk - pr.Tq;
+  bp.q_tiles = pr.q_tiles();
+  bp.Tq_pad = pr.Tq_pad();
+  bp.scale = pr.scale;
+  bp.scale_log2 = pr.scale * 1.4426950408889634f;
+  if (pr.d == 64)
+    e = pr.causal ? launch_main_t<64, true>(pr, maps, bp, stream) : launch_main_t<64, false>(pr, maps, bp, stream);
+  else
+    e = pr.causal ? launch_main_t<128, true>(pr, maps, bp, stream) : launch_main_t<128, false>(pr, maps, bp, stream);
+  if (e != cudaSuccess) return e;
+  ++*launches;
+  }
+
+  // 3. dQ cast
+  if (!(stages & FA_BWD_CAST)) return cudaSuccess;
+  const long long n_vec = q_rows * pr.d / 8;
+  if (pr.d == 64)
+    fa_dq_cast<64><<<grid_for(n_vec, 256), 256, 0, stream>>>(dq_acc, static_cast<uint16_t*>(dQ), n_vec, pr.Tq,
+                                                             pr.Tq_pad(), pr.scale);
+  else
+    fa_dq_cast<128><<<grid_for(n_vec, 256), 256, 0, stream>>>(dq_acc, static_cast<uint16_t*>(dQ), n_vec, pr.Tq,
+                                                              pr.Tq_pad(), pr.scale);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) ++*launches;
+  return e;
+}
+
+}  // namespace fa

@@ -1,0 +1,44 @@
+// Host-side glue shared by the forward, backward and API translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+constexpr int kTile = 128;  // rows of a query tile and of a key/value tile
+
+struct Problem {
+  int B, Hq, Hkv, Tq, Tk, d;
+  int causal;
+  float scale;  // resolved (> 0)
+  int G() const { return Hq / Hkv; }
+  int q_tiles() const { return (Tq + kTile - 1) / kTile; }
+  int kv_tiles() const { return (Tk + kTile - 1) / kTile; }
+  long long Tq_pad() const { return (long long)q_tiles() * kTile; }
+};
+
+// Encodes a TMA descriptor for a contiguous bf16 tensor viewed as
+// [outer][rows][inner] (inner contiguous), box = 64 x 128 x 1, 128-byte swizzle.
+// Returns false if the driver rejects it.
+bool encode_rows_bf16(CUtensorMap* map, const void* base, int inner, int rows, long long outer);
+
+// Device status word of the current device (see fa_last_device_status).
+int* device_status_word();
+
+// Launchers.  Each returns the first CUDA error it met and adds the number
+// of kernels it enqueued to *launches.
+cudaError_t launch_forward(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
+                           cudaStream_t stream, int* launches);
+cudaError_t launch_backward(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
+                            const void* dO, const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                            int stages, cudaStream_t stream, int* launches);
+
+// Workspace carve-up of fa_backward (byte offsets, 256-aligned).
+struct BwdWorkspace {
+  size_t dq_acc, lse2, delta, total;
+};
+BwdWorkspace backward_workspace_layout(const Problem& p);
+
+}  // namespace fa
