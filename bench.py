@@ -28,6 +28,29 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
+
+# DRAM bytes (read + write) of one launch of the dominant kernel on the headline
+# workload, from one ncu capture (profiles/fa_bwd_main_<workload>.md).  Valid
+# only for the source it was taken on: reported as null once that changes.
+NCU_TRAFFIC = {
+    "gqa_B2_H32x8_T8192_d128_causal": {"bytes": 2379315000 + 1156660000, "source_sha256_16": "05f793c80d91fb73"},
+}
+TRAFFIC_SOURCES = ("tiled_attention_05_gb300/csrc/fa_bwd.cu", "tiled_attention_05_gb300/csrc/sm103_ptx.cuh")
+
+
+def measured_traffic(workload: str):
+    import hashlib
+
+    rec = NCU_TRAFFIC.get(workload)
+    if rec is None:
+        return None
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return rec["bytes"] if h.hexdigest()[:16] == rec["source_sha256_16"] else None
+
+
 FLUSH_BYTES = 256 << 20
 
 
@@ -138,34 +161,47 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle legs
-def oracle_sample(w, rows: int | None):
+def oracle_sample(w, rows: int | None, group: int = 0):
     """A bounded sample of the workload for the float64 oracle: one GQA group
-    (batch 0, kv head 0, its G query heads) over the first `rows` tokens
-    (a causal prefix, or the first `rows` queries against all keys)."""
-    from tiled_attention_05_gb300.inputs import make_custom
+    (batch group // Hkv, kv head group % Hkv, its G query heads) over all rows,
+    or over the first `rows` tokens (a causal prefix, or the first `rows`
+    queries against all keys).  Inputs are drawn with the workload's seed plus
+    the group index."""
+    from tiled_attention_05_gb300.inputs import Workload, make_custom
 
     G = w.G
     Tq = w.Tq if rows is None else min(rows, w.Tq)
     Tk = w.Tk if (rows is None or not w.causal) else min(rows, w.Tk)
     if w.causal and w.Tq != w.Tk and rows is not None:
         Tk = w.Tk - (w.Tq - Tq)
-    Q, K, V, dO = make_custom(1, G, 1, Tq, Tk, w.d, w.causal, seed=w.seed, dO_std=w.dO_std)
-    from tiled_attention_05_gb300.inputs import Workload
-
+    Q, K, V, dO = make_custom(1, G, 1, Tq, Tk, w.d, w.causal, seed=w.seed + 1000 * group, dO_std=w.dO_std)
     sw = Workload("sample", 1, G, 1, Tq, Tk, w.d, w.causal, w.seed)
     return (Q, K, V, dO), sw
 
 
-def time_oracle(w, rows, nthreads):
+def time_oracle(w, rows, nthreads, group: int = 0):
     import oracle
 
-    (Q, K, V, dO), sw = oracle_sample(w, rows)
+    (Q, K, V, dO), sw = oracle_sample(w, rows, group)
     Qn, Kn, Vn, dOn = (oracle._f64(t) for t in (Q, K, V, dO))
     t0 = time.perf_counter()
     oracle.forward(Qn, Kn, Vn, w.causal, nthreads=nthreads)
     oracle.backward(Qn, Kn, Vn, dOn, w.causal, nthreads=nthreads)
     dt = time.perf_counter() - t0
     return sw.flops("fwdbwd"), dt, sw
+
+
+def cpu_baseline_leg(w, cores, min_seconds=10.0):
+    """Oracle fwd+bwd over whole GQA groups of the workload until `min_seconds`
+    of CPU work (or every group) is done."""
+    flops, secs, n = 0.0, 0.0, 0
+    groups = w.B * w.Hkv
+    while n < groups and secs < min_seconds:
+        f, dt, sw = time_oracle(w, None, cores, group=n)
+        flops, secs, n = flops + f, secs + dt, n + 1
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {groups} GQA groups ({w.G} query heads each, all {w.Tq} rows, Tk={w.Tk}); "
+                      f"float64 forward + backward; {secs:.1f} s"}
 
 
 def host_cores():
@@ -327,11 +363,7 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cores = host_cores()
-        f, dt, sw = time_oracle(w, None, cores)
-        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": f"one GQA group (batch 0, kv head 0, {w.G} query heads, all {sw.Tq} rows); "
-                         f"float64 forward + backward; {dt:.1f} s"}
+        cpu = cpu_baseline_leg(w, host_cores())
 
     peak = peaks["bf16_tflops"]
     frac = main_tflops / peak
@@ -350,7 +382,7 @@ def run_ours(args, w):
             "bwd_stage_ms": {"pre": statistics.mean(pre_ms), "main": statistics.mean(main_ms),
                              "cast": statistics.mean(cast_ms)},
             "roofline": {"kernel": "fa_bwd_main", "bound": "tensor", "achieved": main_tflops, "peak": peak,
-                         "unit": "TFLOP/s", "frac": frac, "traffic": None,
+                         "unit": "TFLOP/s", "frac": frac, "traffic": measured_traffic(w.name),
                          "peak_source": f"{peaks['source']} bf16 burst"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

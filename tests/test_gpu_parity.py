@@ -139,11 +139,11 @@ def test_saved_state_is_O_and_L_only(fa):
 
     with torch.autograd.graph.saved_tensors_hooks(pack, lambda t: t):
         O = fa.attention(Q, K, V, True)
-        (O.float() * dO.float()).sum().backward()
+        O.backward(dO)  # no loss op of our own: only what the attention function saved is counted
     want = oracle.saved_bytes("keep_o_l", B, Hq, Hkv, T, T, d, d, elem_bytes=2, stat_bytes=4)
     assert total[0] == want
     dense = oracle.saved_bytes("dense", B, Hq, Hkv, T, T, d, d, elem_bytes=2, prob_bytes=2)
-    assert total[0] < dense / 5
+    assert total[0] < dense  # the quadratic softmax output is not kept
 
 
 # ------------------------------------------------------------------ full-size workloads

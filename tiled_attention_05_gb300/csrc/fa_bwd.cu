@@ -19,21 +19,25 @@
 //                accumulator in global memory.
 //   fa_dq_cast   dQ = bf16(scale * accumulator).  HBM-bound.
 //
-// fa_bwd_main roles (320 threads):
-//   warp 0      TMA: K, V once; then Q_t, dO_t (+ the tile's L and D slices by
-//               1-D bulk copy) through a 2-deep ring.
+// fa_bwd_main roles (512 threads, four warpgroups):
+//   warp 0      TMA: K, V once; then Q_t (+ the tile's L and D slices by 1-D
+//               bulk copy) through a 2-deep ring and dO_t through one buffer.
 //   warp 1      tcgen05 issuer, per tile t:
-//                 S^T  = K Q_t^T        -> TMEM [0,128)      (kv rows = lanes)
+//                 S^T  = K Q_t^T        -> TMEM [0,128)      (key rows = lanes)
 //                 dP^T = V dO_t^T       -> TMEM [128,256)
 //                 dV  += P^T dO_t       A = P^T from TMEM (bf16, written over S^T)
 //                 dK  += dS^T Q_t       A = dS^T from shared memory (K-major)
 //                 dQ_t = dS K           -> TMEM [128,128+d)  A = the same dS bytes
 //                                        read MN-major; B = K read MN-major
-//   warps 2..9  two elementwise warpgroups (thread = key row = TMEM lane; group
-//               w owns query columns [64w, 64w+64)): P = exp2(S*scale*log2e - L2),
-//               masks; dS = P * (dP - D) -> shared memory; then drain their
-//               half of dQ_t from TMEM with vector fp32 reductions to global.
+//   warps 4..11 two elementwise warpgroups (thread = key row = TMEM lane; group
+//               w owns query columns [64w, 64w+64)): P = exp2(S*scale*log2e - L2)
+//               with masks -> TMEM; dS = P * (dP - D) -> shared memory.
 //               Epilogue: dV and dK*scale -> bf16 -> TMA store.
+//   warps 12..15 dQ warpgroup (thread = query row): copies dQ_t out of TMEM in
+//               32-column chunks into a 128B-swizzled fp32 staging buffer
+//               (two 16 KB slots) and adds each chunk into the fp32 accumulator
+//               in global memory with one TMA bulk reduce-add.
+// dS uses the bf16-rounded P that also feeds the dV MMA.
 // TMEM columns: S^T/P [0,128), dP^T/dQ [128,256), dV [256,256+d), dK [256+d, 256+2d).
 #include <cstdint>
 
@@ -46,27 +50,28 @@ namespace {
 
 constexpr int BM = fa::kTile;  // query rows per tile
 constexpr int BN = fa::kTile;  // keys per CTA
-constexpr int kThreads = 320;
+constexpr int kThreads = 512;
 
 template <int HD>
 struct BwdCfg {
   static constexpr int TILE = 128 * HD * 2;  // one Q, dO, K or V tile (bf16)
   static constexpr int DS_BYTES = BN * BM * 2;
+  static constexpr int STG_SLOT = 128 * 32 * 4;  // 128 rows x 32 fp32 columns
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
-  static constexpr int OFF_Q = OFF_V + TILE;    // [2]
-  static constexpr int OFF_DO = OFF_Q + 2 * TILE;  // [2]
-  static constexpr int OFF_DS = OFF_DO + 2 * TILE;
-  static constexpr int OFF_LSE = OFF_DS + DS_BYTES;    // [2][128] fp32
+  static constexpr int OFF_Q = OFF_V + TILE;       // [2]
+  static constexpr int OFF_DO = OFF_Q + 2 * TILE;  // [1]
+  static constexpr int OFF_DS = OFF_DO + TILE;
+  static constexpr int OFF_STG = OFF_DS + DS_BYTES;    // [2] dQ staging slots
+  static constexpr int OFF_LSE = OFF_STG + 2 * STG_SLOT;  // [2][128] fp32
   static constexpr int OFF_DELTA = OFF_LSE + 2 * 512;  // [2][128] fp32
   static constexpr int OFF_BAR = OFF_DELTA + 2 * 512;
-  static constexpr int NBAR = 16;
+  static constexpr int NBAR = 24;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct BwdParams {
-  float* dq_acc;
   const float* lse2;
   const float* delta;
   int* status;
@@ -80,22 +85,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
-                const BwdParams p) {
+                const __grid_constant__ CUtensorMap tmAcc, const BwdParams p) {
   using C = BwdCfg<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars + 0;
-  uint64_t* qdo_full = bars + 1;   // [2]
-  uint64_t* qdo_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;
-  uint64_t* dp_full = bars + 6;
-  uint64_t* p_ready = bars + 7;
-  uint64_t* ds_ready = bars + 8;
-  uint64_t* tS_free = bars + 9;
-  uint64_t* dq_full = bars + 10;
-  uint64_t* dq_empty = bars + 11;
-  uint64_t* acc_done = bars + 12;
-  uint64_t* drain = bars + 13;
+  uint64_t* q_full = bars + 1;   // [2]
+  uint64_t* q_empty = bars + 3;  // [2]
+  uint64_t* do_full = bars + 5;
+  uint64_t* do_empty = bars + 6;
+  uint64_t* s_full = bars + 7;
+  uint64_t* dp_full = bars + 8;
+  uint64_t* p_ready = bars + 9;
+  uint64_t* ds_ready = bars + 10;
+  uint64_t* tS_free = bars + 11;
+  uint64_t* dq_full = bars + 12;
+  uint64_t* dq_empty = bars + 13;
+  uint64_t* acc_done = bars + 14;
+  uint64_t* drain = bars + 15;
+  uint64_t* stg_full = bars + 16;  // [2]
+  uint64_t* stg_free = bars + 18;  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -117,16 +126,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;
     mbar_init(kv_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&qdo_full[s], 1);
-      mbar_init(&qdo_empty[s], 1);
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+      mbar_init(&stg_full[s], 128);
+      mbar_init(&stg_free[s], 1);
     }
+    mbar_init(do_full, 1);
+    mbar_init(do_empty, 1);
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 256);
     mbar_init(ds_ready, 256);
     mbar_init(tS_free, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 256);
+    mbar_init(dq_empty, 128);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -142,9 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool run = (*abort_flag == 0) && T > 0;
   const uint32_t T_S = tmem, T_DP = tmem + 128, T_DV = tmem + 256, T_DK = tmem + 256 + HD;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && run) {
+  if (warp < 4) {
+    if (warp == 0 && lane == 0 && run) {
+      // ---------------------------------------------------------- producer
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmdO);
       mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
@@ -153,41 +166,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem + C::OFF_K + cb * BN * 128, &tmK, kv_full, cb * 64, k0, bkv);
         tma_load_3d(smem + C::OFF_V + cb * BN * 128, &tmV, kv_full, cb * 64, k0, bkv);
       }
-      int last[2] = {-1, -1};
+      int last_q[2] = {-1, -1}, last_do = -1;
       for (int t = 0; t < T; ++t) {
         const int st = t & 1, u = t >> 1;
         const int g = t / n_m, m = m_begin + (t - g * n_m);
         const int bh = b * p.Hq + hk * p.G + g;
-        if (!mbar_wait(&qdo_empty[st], (u & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&qdo_full[st], 2 * C::TILE + 1024);
+        if (!mbar_wait(&q_empty[st], (u & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&q_full[st], C::TILE + 1024);
 #pragma unroll
-        for (int cb = 0; cb < HD / 64; ++cb) {
-          tma_load_3d(smem + C::OFF_Q + st * C::TILE + cb * BM * 128, &tmQ, &qdo_full[st], cb * 64, m * BM, bh);
-          tma_load_3d(smem + C::OFF_DO + st * C::TILE + cb * BM * 128, &tmdO, &qdo_full[st], cb * 64, m * BM, bh);
-        }
+        for (int cb = 0; cb < HD / 64; ++cb)
+          tma_load_3d(smem + C::OFF_Q + st * C::TILE + cb * BM * 128, &tmQ, &q_full[st], cb * 64, m * BM, bh);
         const long long row0 = (long long)bh * p.Tq_pad + (long long)m * BM;
-        bulk_load(smem + C::OFF_LSE + st * 512, p.lse2 + row0, 512, &qdo_full[st]);
-        bulk_load(smem + C::OFF_DELTA + st * 512, p.delta + row0, 512, &qdo_full[st]);
-        last[st] = u;
+        bulk_load(smem + C::OFF_LSE + st * 512, p.lse2 + row0, 512, &q_full[st]);
+        bulk_load(smem + C::OFF_DELTA + st * 512, p.delta + row0, 512, &q_full[st]);
+        last_q[st] = u;
+        // dO has one buffer, refilled only once dV_{t-1} is done: pull it into
+        // L2 now so that its load later does not stall the dP MMA.
+#pragma unroll
+        for (int cb = 0; cb < HD / 64; ++cb) tma_prefetch_l2_3d(&tmdO, cb * 64, m * BM, bh);
+        if (!mbar_wait(do_empty, (t & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(do_full, C::TILE);
+#pragma unroll
+        for (int cb = 0; cb < HD / 64; ++cb)
+          tma_load_3d(smem + C::OFF_DO + cb * BM * 128, &tmdO, do_full, cb * 64, m * BM, bh);
+        last_do = t;
       }
       mbar_wait_bounded(kv_full, 0);
       for (int st = 0; st < 2; ++st)
-        if (last[st] >= 0) mbar_wait_bounded(&qdo_full[st], last[st] & 1);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && run) {
+        if (last_q[st] >= 0) mbar_wait_bounded(&q_full[st], last_q[st] & 1);
+      if (last_do >= 0) mbar_wait_bounded(do_full, last_do & 1);
+    } else if (warp == 1 && lane == 0 && run) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t id_sdp = idesc_bf16(BN, BM, 0, 0);  // S^T, dP^T: M = keys, N = queries
       constexpr uint32_t id_kv = idesc_bf16(BN, HD, 0, 1);   // dV, dK: M = keys, N = d, B MN-major
       constexpr uint32_t id_q = idesc_bf16(BM, HD, 1, 1);    // dQ: M = queries (A MN-major), N = d
       const uint32_t k_base = smem_u32(smem + C::OFF_K), v_base = smem_u32(smem + C::OFF_V);
       const uint32_t ds_base = smem_u32(smem + C::OFF_DS);
+      const uint32_t do_base = smem_u32(smem + C::OFF_DO);
       bool ok = mbar_wait(kv_full, 0, abort_flag);
       for (int t = 0; ok && t < T; ++t) {
         const int st = t & 1, u = t >> 1;
         const uint32_t q_base = smem_u32(smem + C::OFF_Q + st * C::TILE);
-        const uint32_t do_base = smem_u32(smem + C::OFF_DO + st * C::TILE);
-        if (!mbar_wait(&qdo_full[st], u & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&q_full[st], u & 1, abort_flag)) { ok = false; break; }
         if (t > 0 && !mbar_wait(tS_free, (t - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
@@ -195,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(T_S, desc_kmajor(k_base + (k >> 2) * (BN * 128) + (k & 3) * 32),
                  desc_kmajor(q_base + (k >> 2) * (BM * 128) + (k & 3) * 32), id_sdp, k > 0 ? 1u : 0u);
         mma_commit(s_full);
+        if (!mbar_wait(do_full, t & 1, abort_flag)) { ok = false; break; }
         if (t > 0 && !mbar_wait(dq_empty, (t - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
@@ -205,20 +226,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(p_ready, t & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         // P^T lives in TMEM as packed bf16: query columns [0,64) at TMEM columns
-        // [0,32), query columns [64,128) at [64,96) (each warpgroup overwrote its
-        // own half of S^T).
+        // [0,32), query columns [64,128) at [64,96) (each elementwise warpgroup
+        // overwrote its own half of S^T).
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
           mma_ts(T_DV, T_S + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(do_base + k * 2048, BM * 128), id_kv,
                  (t > 0 || k > 0) ? 1u : 0u);
         mma_commit(tS_free);
+        mma_commit(do_empty);
         if (!mbar_wait(ds_ready, t & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
           mma_ss(T_DK, desc_kmajor(ds_base + (k >> 2) * (BN * 128) + (k & 3) * 32),
                  desc_mnmajor(q_base + k * 2048, BM * 128), id_kv, (t > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&qdo_empty[st]);
+        mma_commit(&q_empty[st]);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
           mma_ss(T_DP, desc_mnmajor(ds_base + k * 2048, BN * 128), desc_mnmajor(k_base + k * 2048, BN * 128), id_q,
@@ -229,11 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(drain);
       mbar_wait_bounded(drain, 0);
     }
-  } else {
+  } else if (warp < 12) {
     // ------------------------------------------------------------ elementwise warpgroups
-    const int wg = (warp - 2) >> 2;  // 0 or 1
+    const int wg = (warp - 4) >> 2;  // 0 or 1
     const int quad = warp & 3;
-    const int r = quad * 32 + lane;  // TMEM lane: key row for S^T/dP^T/dV/dK, query row for dQ
+    const int r = quad * 32 + lane;  // TMEM lane = key row
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const int key = k0 + r;
     const bool key_valid = key < p.Tk;
@@ -242,75 +264,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; ok && t < T; ++t) {
       const int st = t & 1, u = t >> 1;
       const int g = t / n_m, m = m_begin + (t - g * n_m);
-      const int bh = b * p.Hq + hk * p.G + g;
       const int q0 = m * BM;
       const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE + st * 512);
       const float* del_s = reinterpret_cast<const float*>(smem + C::OFF_DELTA + st * 512);
-      if (!mbar_wait(&qdo_full[st], u & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(&q_full[st], u & 1, abort_flag)) { ok = false; break; }
       if (!mbar_wait(s_full, t & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      // ---- P = exp2(S * scale * log2e - L2), masked
-      uint32_t sr[64];
-      tmem_ld32(T_S + lane_base + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(T_S + lane_base + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_wait_ld();
+      // ---- P = exp2(S * scale * log2e - L2), masked; 32 query columns at a time.
+      // The packed bf16 P of chunk c is stored over S columns this thread has
+      // already read (each thread only touches its own TMEM lane).
       const bool need_mask = !key_valid || (CAUSAL && k0 + BN - 1 > q0 + p.causal_off);
       // key row `key` is visible to query q0 + c iff key <= q0 + c + off
       const int vis_from = key_valid ? (CAUSAL ? key - p.causal_off - q0 : -0x40000000) : 0x40000000;
-      float pr[64];
+      uint32_t pk[32];  // P as packed bf16 pairs, query columns wg*64 .. wg*64+63
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int qc = wg * 64 + c;
-        float v = ex2(fmaf(__uint_as_float(sr[c]), sl2, -lse_s[qc]));
-        if (need_mask && qc < vis_from) v = 0.f;
-        pr[c] = v;
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t sr[32];
+        tmem_ld32(T_S + lane_base + wg * 64 + ch * 32, sr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const int qc = wg * 64 + ch * 32 + c;
+          float v0 = ex2(fmaf(__uint_as_float(sr[c]), sl2, -lse_s[qc]));
+          float v1 = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, -lse_s[qc + 1]));
+          if (need_mask) {
+            if (qc < vis_from) v0 = 0.f;
+            if (qc + 1 < vis_from) v1 = 0.f;
+          }
+          pk[ch * 16 + c / 2] = pack_bf16x2(v0, v1);
+        }
+        tmem_st16(T_S + lane_base + wg * 64 + ch * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[ch * 16]));
       }
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
-      tmem_st32(T_S + lane_base + wg * 64, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_ready);
       // ---- dS = P * (dP - D) -> shared memory (row = key, 128B-swizzled, query-contiguous)
       if (!mbar_wait(dp_full, t & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      uint32_t dr[64];
-      tmem_ld32(T_DP + lane_base + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-      tmem_ld32(T_DP + lane_base + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
-      tmem_wait_ld();
+      // the dK / dQ MMAs of the previous tile must be done reading dS
+      if (t > 0 && !mbar_wait(dq_full, (t - 1) & 1, abort_flag)) { ok = false; break; }
       uint8_t* ds_blk = smem + C::OFF_DS + wg * (BN * 128);
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        uint32_t w[4];
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t dr[32];
+        tmem_ld32(T_DP + lane_base + wg * 64 + ch * 32, dr);
+        tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = cc * 8 + 2 * e;
-          const float d0 = pr[c] * (__uint_as_float(dr[c]) - del_s[wg * 64 + c]);
-          const float d1 = pr[c + 1] * (__uint_as_float(dr[c + 1]) - del_s[wg * 64 + c + 1]);
-          w[e] = pack_bf16x2(d0, d1);
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = cc * 8 + 2 * e;           // column inside the chunk
+            const int qc = wg * 64 + ch * 32 + c;   // query column inside the tile
+            const uint32_t pp = pk[ch * 16 + c / 2];
+            const float p0 = __uint_as_float(pp << 16), p1 = __uint_as_float(pp & 0xffff0000u);
+            const float d0 = p0 * (__uint_as_float(dr[c]) - del_s[qc]);
+            const float d1 = p1 * (__uint_as_float(dr[c + 1]) - del_s[qc + 1]);
+            w[e] = pack_bf16x2(d0, d1);
+          }
+          st_shared_v4(smem_u32(ds_blk + sw128_offset(r, ch * 4 + cc)), w[0], w[1], w[2], w[3]);
         }
-        st_shared_v4(smem_u32(ds_blk + sw128_offset(r, cc)), w[0], w[1], w[2], w[3]);
       }
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(ds_ready);
-      // ---- drain this warpgroup's half of dQ_t (TMEM lane = query row) into the fp32 accumulator
-      if (!mbar_wait(dq_full, t & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      constexpr int HALF = HD / 2;
-      uint32_t qr[HALF];
-#pragma unroll
-      for (int c = 0; c < HALF / 32; ++c)
-        tmem_ld32(T_DP + lane_base + wg * HALF + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&qr[c * 32]));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(dq_empty);
-      float* dst = p.dq_acc + ((long long)bh * p.Tq_pad + q0 + r) * HD + wg * HALF;
-#pragma unroll
-      for (int c = 0; c < HALF; c += 4)
-        red_add_v4(dst + c, __uint_as_float(qr[c]), __uint_as_float(qr[c + 1]), __uint_as_float(qr[c + 2]),
-                   __uint_as_float(qr[c + 3]));
     }
     // ---- epilogue: dV, dK * scale -> bf16 -> shared (the Q ring, idle now) -> TMA store
     if (ok && T > 0) {
@@ -350,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();
       named_bar_sync(2, 256);
-      if (warp == 2 && lane == 0) {
+      if (warp == 4 && lane == 0) {
         prefetch_tmap(&tmdV);
         prefetch_tmap(&tmdK);
 #pragma unroll
@@ -362,6 +379,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_wait0();
       }
     }
+  } else {
+    // ------------------------------------------------------------ dQ warpgroup
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // TMEM lane = query row of the tile
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const bool leader = (warp == 12 && lane == 0);
+    constexpr int NCH = HD / 32;  // 32-column chunks per tile, drained two at a time
+    bool ok = run;
+    int k = 0;  // chunks staged so far; chunk k uses slot k & 1
+    // Stage one 32-column chunk (already in registers) into its slot and let the
+    // leader add it into the accumulator.  A slot is reused two chunks later;
+    // the leader confirms that the copy out of it has been read only then, so
+    // the bulk read overlaps the next chunk.
+    auto stage = [&](const uint32_t (&v)[32], int col, int row0, int bh) -> bool {
+      const int slot = k & 1;
+      if (k >= 2) {
+        if (leader) {
+          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // chunk k-2 read
+          mbar_arrive(&stg_free[slot]);
+        }
+        if (!mbar_wait(&stg_free[slot], ((k >> 1) - 1) & 1, abort_flag)) return false;
+      }
+      uint8_t* stg = smem + C::OFF_STG + slot * C::STG_SLOT;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_shared_v4(smem_u32(stg + sw128_offset(r, q)), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      fence_async_smem();
+      mbar_arrive(&stg_full[slot]);
+      if (leader) {
+        if (!mbar_wait(&stg_full[slot], (k >> 1) & 1, abort_flag)) return false;
+        tma_reduce_add_3d(&tmAcc, stg, col, row0, bh);
+        bulk_commit();
+      }
+      ++k;
+      return true;
+    };
+    for (int t = 0; ok && t < T; ++t) {
+      const int g = t / n_m, m = m_begin + (t - g * n_m);
+      const int bh = b * p.Hq + hk * p.G + g;
+      if (!mbar_wait(dq_full, t & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      for (int c = 0; ok && c < NCH; c += 2) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(T_DP + lane_base + c * 32, v0);
+        if (c + 1 < NCH) tmem_ld32(T_DP + lane_base + (c + 1) * 32, v1);
+        tmem_wait_ld();
+        if (c + 2 >= NCH) {
+          tc_fence_before();
+          mbar_arrive(dq_empty);  // all of dQ_t is out of TMEM: it may take dP_{t+1}
+        }
+        if (!stage(v0, c * 32, m * BM, bh)) { ok = false; break; }
+        if (c + 1 < NCH && !stage(v1, (c + 1) * 32, m * BM, bh)) { ok = false; break; }
+      }
+    }
+    if (leader) bulk_wait0();  // every reduce-add has landed before the kernel ends
   }
   tc_fence_before();
   __syncthreads();
@@ -458,7 +530,7 @@ cudaError_t launch_main_t(const fa::Problem& pr, const CUtensorMap* maps, const 
   }
   dim3 grid(pr.B * pr.Hkv, pr.kv_tiles());
   fa_bwd_main<HD, CAUSAL><<<grid, kThreads, C::SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
-                                                               bp);
+                                                               maps[6], bp);
   return cudaGetLastError();
 }
 
@@ -531,16 +603,16 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
 
   // 2. main
   if (stages & FA_BWD_MAIN) {
-  CUtensorMap maps[6];
+  CUtensorMap maps[7];
   if (!encode_rows_bf16(&maps[0], Q, pr.d, pr.Tq, (long long)pr.B * pr.Hq) ||
       !encode_rows_bf16(&maps[1], K, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
       !encode_rows_bf16(&maps[2], V, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
       !encode_rows_bf16(&maps[3], dO, pr.d, pr.Tq, (long long)pr.B * pr.Hq) ||
       !encode_rows_bf16(&maps[4], dK, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
-      !encode_rows_bf16(&maps[5], dV, pr.d, pr.Tk, (long long)pr.B * pr.Hkv))
+      !encode_rows_bf16(&maps[5], dV, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
+      !encode_acc_f32(&maps[6], dq_acc, pr.d, pr.Tq_pad(), (long long)pr.B * pr.Hq))
     return cudaErrorInvalidValue;
   BwdParams bp;
-  bp.dq_acc = dq_acc;
   bp.lse2 = lse2;
   bp.delta = delta;
   bp.status = device_status_word();

@@ -7,17 +7,24 @@
 // output when the maximum moves; normalise once at the end and emit
 // L = m + log(l) beside O.  Nothing of size Tq x Tk is ever stored.
 //
-// GB300 mapping (one CTA = one 128-row query tile of one (batch, head)):
-//   warp 0      TMA producer: Q once, then K_j / V_j through an NS-deep ring.
-//   warp 1      tcgen05 issuer: S_j = Q K_j^T into one of two TMEM score
-//               buffers, then O += P_{j-1} V_{j-1} into the TMEM accumulator.
-//   warps 2..5  softmax (thread = query row = TMEM lane): load the score row
-//               from TMEM, mask, row max, exp2, row sum, write P (bf16) to
-//               shared memory in the 128B-swizzled K-major layout the next
-//               MMA reads; rescale the O row in TMEM when its max grows by
-//               more than 2^8 (lazy rescaling: exact after normalisation);
-//               epilogue O / l -> bf16 -> TMA store, L -> global.
-// TMEM: S buffers at columns [0,128) and [128,256), O at [256, 256+d).
+// GB300 mapping: one CTA = two 128-row query tiles (A and B) of one
+// (batch, head), sharing every K/V tile it loads.
+//   warp 0       TMA producer: Q_A and Q_B once, then K_j / V_j through NS-deep rings.
+//   warp 1       tcgen05 issuer.  Per key tile j it issues, in this order,
+//                  O_A += P_A(j) V_j,  S_A(j+1) = Q_A K_{j+1}^T,
+//                  O_B += P_B(j) V_j,  S_B(j+1) = Q_B K_{j+1}^T,
+//                so while one softmax warpgroup works on its tile the tensor
+//                pipe runs the other tile's two MMAs (ping-pong).  P is read
+//                straight from TMEM (A operand); the MMAs of one thread execute
+//                in issue order, so S_X(j+1) overwrites P_X(j) only after the
+//                P.V that reads it.
+//   warps 4..7   softmax of tile A, warps 8..11 softmax of tile B (thread =
+//                query row = TMEM lane): load the score row, mask, row max,
+//                exp2, row sum, write P as packed bf16 over the scores in TMEM;
+//                rescale the O row in TMEM when the max grows by more than 2^8
+//                (lazy rescaling, exact after the final normalisation);
+//                epilogue O / l -> bf16 -> TMA store, L -> global.
+// TMEM columns: S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,256+d), O_B [384,384+d).
 // Scores are kept in log2 units (scale * log2(e) folded into one FMA).
 #include <cstdint>
 
@@ -28,9 +35,9 @@ using namespace fa_ptx;
 
 namespace {
 
-constexpr int BM = fa::kTile;  // query rows per CTA
+constexpr int BM = fa::kTile;  // query rows per tile (two tiles per CTA)
 constexpr int BN = fa::kTile;  // keys per tile
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256 between rescales
 
 template <int HD>
@@ -38,13 +45,11 @@ struct FwdCfg {
   static constexpr int NS = HD == 64 ? 4 : 2;  // K/V ring depth
   static constexpr int Q_BYTES = BM * HD * 2;
   static constexpr int KV_BYTES = BN * HD * 2;
-  static constexpr int P_BYTES = BM * BN * 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_Q = 0;  // [2]: tile A, tile B
+  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NS * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + NS * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  static constexpr int NBAR = 1 + 4 * NS + 2 + 2 + 1 + 1 + 1;
+  static constexpr int OFF_BAR = OFF_V + NS * KV_BYTES;
+  static constexpr int NBAR = 1 + 4 * NS + 2 + 2 + 2 + 1;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -57,6 +62,15 @@ struct FwdParams {
   int kv_tiles;
   float scale_log2;  // scale * log2(e)
 };
+
+// Key tiles that query rows [qa, qa+128) must visit.
+template <bool CAUSAL>
+__device__ __forceinline__ int kv_tiles_for(const FwdParams& p, int qa) {
+  if (qa >= p.Tq) return 0;
+  if (!CAUSAL) return p.kv_tiles;
+  const int last_key = min(qa + BM, p.Tq) - 1 + p.causal_off;  // last key the tile's last row sees
+  return last_key < 0 ? 0 : min(p.kv_tiles, last_key / BN + 1);
+}
 
 template <int HD, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -72,26 +86,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = k_full + NS;
   uint64_t* v_full = k_empty + NS;
   uint64_t* v_empty = v_full + NS;
-  uint64_t* s_full = v_empty + NS;  // [2]
-  uint64_t* s_empty = s_full + 2;   // [2]
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* pv_done = p_full + 1;
-  uint64_t* drain = pv_done + 1;
+  uint64_t* s_full = v_empty + NS;  // [2] per tile
+  uint64_t* p_full = s_full + 2;    // [2]
+  uint64_t* o_done = p_full + 2;    // [2]
+  uint64_t* drain = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
   const int b = bh / p.Hq, h = bh - b * p.Hq;
-  const int qt = gridDim.y - 1 - blockIdx.y;  // longest causal rows first
-  const int q0 = qt * BM;
+  const int q0 = (gridDim.y - 1 - blockIdx.y) * (2 * BM);  // longest causal rows first
   const int bkv = b * p.Hkv + h / p.G;
-
-  int nkv = p.kv_tiles;
-  if (CAUSAL) {
-    const int last_key = min(q0 + BM, p.Tq) - 1 + p.causal_off;  // last key the tile's last row sees
-    nkv = last_key < 0 ? 0 : min(nkv, last_key / BN + 1);
-  }
+  const int nkv_t[2] = {kv_tiles_for<CAUSAL>(p, q0), kv_tiles_for<CAUSAL>(p, q0 + BM)};
+  const int nkv_max = max(nkv_t[0], nkv_t[1]);
+  const bool has_b = q0 + BM < p.Tq;
 
   if (threadIdx.x == 0) {
     *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;  // swizzled tiles need 1024 B alignment
@@ -102,12 +111,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 128);
+      mbar_init(&o_done[x], 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(pv_done, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
   }
@@ -119,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const bool run = (*abort_flag == 0) && nkv > 0;
+  const bool run = (*abort_flag == 0) && nkv_max > 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -127,13 +135,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+      mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_BYTES);
 #pragma unroll
-      for (int cb = 0; cb < HD / 64; ++cb) tma_load_3d(smem + C::OFF_Q + cb * BM * 128, &tmQ, q_full, cb * 64, q0, bh);
+      for (int cb = 0; cb < HD / 64; ++cb) {
+        tma_load_3d(smem + C::OFF_Q + cb * BM * 128, &tmQ, q_full, cb * 64, q0, bh);
+        if (has_b) tma_load_3d(smem + C::OFF_Q + C::Q_BYTES + cb * BM * 128, &tmQ, q_full, cb * 64, q0 + BM, bh);
+      }
       int k_last[NS], v_last[NS];
 #pragma unroll
       for (int s = 0; s < NS; ++s) k_last[s] = v_last[s] = -1;
-      for (int j = 0; j < nkv; ++j) {
+      for (int j = 0; j < nkv_max; ++j) {
         const int s = j % NS, u = j / NS;
         if (!mbar_wait(&k_empty[s], (u & 1) ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(&k_full[s], C::KV_BYTES);
@@ -161,104 +172,115 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && run) {
       constexpr uint32_t idS = idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idPV = idesc_bf16(BM, HD, 0, 1);
-      const uint32_t tO = tmem + 256;
-      const uint32_t q_base = smem_u32(smem + C::OFF_Q);
       const uint32_t k_base = smem_u32(smem + C::OFF_K);
       const uint32_t v_base = smem_u32(smem + C::OFF_V);
-      const uint32_t p_base = smem_u32(smem + C::OFF_P);
-      auto issue_pv = [&](int t) -> bool {
-        const int s = t % NS, u = t / NS;
-        if (!mbar_wait(p_full, t & 1, abort_flag)) return false;
-        if (!mbar_wait(&v_full[s], u & 1, abort_flag)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t a = desc_kmajor(p_base + (k >> 2) * (BM * 128) + (k & 3) * 32);
-          const uint64_t bd = desc_mnmajor(v_base + s * C::KV_BYTES + k * 2048, BN * 128);
-          mma_ss(tO, a, bd, idPV, (t > 0 || k > 0) ? 1u : 0u);
-        }
-        mma_commit(pv_done);
-        mma_commit(&v_empty[s]);
-        return true;
-      };
       bool ok = mbar_wait(q_full, 0, abort_flag);
       if (ok) tc_fence_after();
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % NS, u = j / NS, sb = j & 1;
-        if (!mbar_wait(&k_full[s], u & 1, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(&s_empty[sb], ((j >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+      // S_X(j) = Q_X K_j^T into TMEM [128 X, 128 X + 128)
+      auto issue_s = [&](int x, int j) -> bool {
+        const int s = j % NS;
+        if (!mbar_wait(&k_full[s], (j / NS) & 1, abort_flag)) return false;
         tc_fence_after();
+        const uint32_t q_base = smem_u32(smem + C::OFF_Q + x * C::Q_BYTES);
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint64_t a = desc_kmajor(q_base + (k >> 2) * (BM * 128) + (k & 3) * 32);
           const uint64_t bd = desc_kmajor(k_base + s * C::KV_BYTES + (k >> 2) * (BN * 128) + (k & 3) * 32);
-          mma_ss(tmem + sb * 128, a, bd, idS, k > 0 ? 1u : 0u);
+          mma_ss(tmem + x * 128, a, bd, idS, k > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[sb]);
-        mma_commit(&k_empty[s]);
-        if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+        mma_commit(&s_full[x]);
+        return true;
+      };
+      // O_X += P_X(j) V_j with P_X read from TMEM (packed bf16 over S_X)
+      auto issue_pv = [&](int x, int j) -> bool {
+        const int s = j % NS;
+        if (!mbar_wait(&p_full[x], j & 1, abort_flag)) return false;
+        if (!mbar_wait(&v_full[s], (j / NS) & 1, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint64_t bd = desc_mnmajor(v_base + s * C::KV_BYTES + k * 2048, BN * 128);
+          mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, bd, idPV, (j > 0 || k > 0) ? 1u : 0u);
+        }
+        return true;
+      };
+      if (ok && nkv_t[0] > 0) ok = issue_s(0, 0);
+      if (ok && nkv_t[1] > 0) ok = issue_s(1, 0);
+      if (ok) mma_commit(&k_empty[0]);
+      for (int j = 0; ok && j < nkv_max; ++j) {
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (j < nkv_t[x]) {
+            if (!issue_pv(x, j)) { ok = false; break; }
+            if (x == 1 || j >= nkv_t[1]) mma_commit(&v_empty[j % NS]);  // last reader of V_j
+            if (j + 1 < nkv_t[x]) {
+              if (!issue_s(x, j + 1)) { ok = false; break; }
+              if (x == 1 || j + 1 >= nkv_t[1]) mma_commit(&k_empty[(j + 1) % NS]);  // last reader of K_{j+1}
+            } else {
+              mma_commit(&o_done[x]);
+            }
+          }
+        }
       }
-      if (ok) issue_pv(nkv - 1);
       // Let every MMA issued above finish before TMEM is released.
       mma_commit(drain);
       mbar_wait_bounded(drain, 0);
     }
-  } else {
-    // ------------------------------------------------------------ softmax + epilogue
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue of tile x
+    const int x = (warp - 4) >> 2;
+    const int nkv = nkv_t[x];
+    const int qx0 = q0 + x * BM;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // row inside the tile == TMEM lane
-    const int i = q0 + r;            // query row
+    const int i = qx0 + r;           // query row
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t tS = tmem + x * 128 + lane_base;
+    const uint32_t tO = tmem + 256 + x * 128 + lane_base;
     const float sl2 = p.scale_log2;
     const float NEG_INF = -__int_as_float(0x7f800000);
     float m_ref = NEG_INF;  // reference max (log2 units) the P values are taken against
     float l = 0.f;
     bool ok = run;
-    uint8_t* Ps = smem + C::OFF_P;
     for (int j = 0; ok && j < nkv; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(&s_full[x], j & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[BN];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c)
-        tmem_ld32(tmem + sb * 128 + lane_base + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&s_empty[sb]);
-      float s[BN];
-#pragma unroll
-      for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
       const int kv0 = j * BN;
-      const bool need_mask = (kv0 + BN > p.Tk) || (CAUSAL && kv0 + BN - 1 > q0 + p.causal_off);
+      const bool need_mask = (kv0 + BN > p.Tk) || (CAUSAL && kv0 + BN - 1 > qx0 + p.causal_off);
       if (need_mask) {
         int lim = p.Tk - kv0;
         if (CAUSAL) lim = min(lim, i + p.causal_off + 1 - kv0);
 #pragma unroll
         for (int c = 0; c < BN; ++c)
-          if (c >= lim) s[c] = NEG_INF;
+          if (c >= lim) sr[c] = __float_as_uint(NEG_INF);
       }
-      float mt = s[0];
+      float mt = __uint_as_float(sr[0]);
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mt = fmaxf(mt, s[c]);
+      for (int c = 1; c < BN; ++c) mt = fmaxf(mt, __uint_as_float(sr[c]));
       const float mt2 = mt * sl2;
       float m_new = m_ref;
       if (mt2 > m_ref + kRescaleThreshold) m_new = mt2;  // also taken when m_ref == -inf
       const float base = (m_new == NEG_INF) ? 0.f : m_new;
-      uint32_t pk[BN / 2];
+      // exponentials; P (packed bf16 pairs) goes over the already-loaded scores
+      // in TMEM 16 columns at a time, so few registers hold it
       float rowsum = 0.f;
 #pragma unroll
-      for (int c = 0; c < BN; c += 2) {
-        const float e0 = ex2(fmaf(s[c], sl2, -base));
-        const float e1 = ex2(fmaf(s[c + 1], sl2, -base));
-        rowsum += e0 + e1;
-        pk[c / 2] = pack_bf16x2(e0, e1);
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float e0 = ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e]), sl2, -base));
+          const float e1 = ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e + 1]), sl2, -base));
+          rowsum += e0 + e1;
+          pk[e] = pack_bf16x2(e0, e1);
+        }
+        tmem_st16(tS + 16 * c, pk);
       }
-      // The previous P.V must be done before P is overwritten or O rescaled.
-      if (j > 0) {
-        if (!mbar_wait(pv_done, (j - 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-      }
+      // O_X is idle here: the P.V of tile j-1 completed before S_X(j) did.
       if (m_new != m_ref) {
         const float alpha = (m_ref == NEG_INF) ? 0.f : ex2(m_ref - m_new);
         l *= alpha;
@@ -266,42 +288,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t o[32];
-            tmem_ld32(tmem + 256 + lane_base + c * 32, o);
+            tmem_ld32(tO + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tmem + 256 + lane_base + c * 32, o);
+            tmem_st32(tO + c * 32, o);
           }
-          tmem_wait_st();
         }
         m_ref = m_new;
       }
       l += rowsum;
-#pragma unroll
-      for (int cc = 0; cc < BN / 8; ++cc)
-        st_shared_v4(smem_u32(Ps + (cc >> 3) * (BM * 128) + sw128_offset(r, cc & 7)), pk[4 * cc], pk[4 * cc + 1],
-                     pk[4 * cc + 2], pk[4 * cc + 3]);
-      fence_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[x]);
     }
-    // ---- epilogue: O / l -> bf16 -> shared (Q's buffer, free now) -> TMA store; L -> global
-    if (ok) {
-      if (!mbar_wait(pv_done, (nkv - 1) & 1, abort_flag)) ok = false;
+    // ---- epilogue: O / l -> bf16 -> shared (this tile's Q buffer, free now) -> TMA store; L -> global
+    if (ok && nkv > 0) {
+      if (!mbar_wait(&o_done[x], 0, abort_flag)) ok = false;
       tc_fence_after();
     }
-    // All 128 softmax threads agree on whether to write (a timeout anywhere in
-    // the CTA cancels the epilogue), so the barriers below can never split.
-    const bool mine = ((nkv == 0) || ok) && *abort_flag == 0;
-    if (named_bar_and(1, 128, mine)) {
+    // All 128 threads of the warpgroup agree on whether to write (a timeout
+    // anywhere in the CTA cancels the epilogue), so its barriers never split.
+    const bool mine = ((nkv == 0) || ok) && *abort_flag == 0 && qx0 < p.Tq;
+    if (named_bar_and(1 + x, 128, mine)) {
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       if (i < p.Tq) p.L[(size_t)bh * p.Tq + i] = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : NEG_INF;
-      uint8_t* Os = smem + C::OFF_Q;
+      uint8_t* Os = smem + C::OFF_Q + x * C::Q_BYTES;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t o[32];
         if (nkv > 0) {
-          tmem_ld32(tmem + 256 + lane_base + c * 32, o);
+          tmem_ld32(tO + c * 32, o);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -317,11 +334,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       fence_async_smem();
-      named_bar_sync(2, 128);
-      if (warp == 2 && lane == 0) {
+      named_bar_sync(3 + x, 128);
+      if (quad == 0 && lane == 0) {
         prefetch_tmap(&tmO);
 #pragma unroll
-        for (int cb = 0; cb < HD / 64; ++cb) tma_store_3d(&tmO, Os + cb * BM * 128, cb * 64, q0, bh);
+        for (int cb = 0; cb < HD / 64; ++cb) tma_store_3d(&tmO, Os + cb * BM * 128, cb * 64, qx0, bh);
         bulk_commit();
         bulk_wait0();
       }
@@ -358,7 +375,7 @@ cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUt
   p.causal_off = pr.Tk - pr.Tq;
   p.kv_tiles = pr.kv_tiles();
   p.scale_log2 = pr.scale * 1.4426950408889634f;
-  dim3 grid(pr.B * pr.Hq, pr.q_tiles());
+  dim3 grid(pr.B * pr.Hq, (pr.q_tiles() + 1) / 2);
   fa_fwd_kernel<HD, CAUSAL><<<grid, kThreads, C::SMEM, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
