@@ -67,7 +67,8 @@ typedef enum {
   FA_ERR_INVALID_ARG = 1,
   FA_ERR_UNSUPPORTED = 2,
   FA_ERR_CUDA = 3,
-  FA_ERR_TIMEOUT = 4
+  FA_ERR_TIMEOUT = 4,
+  FA_ERR_SCRATCH_TOO_SMALL = 5
 } fa_status;
 
 typedef struct {
@@ -103,6 +104,29 @@ enum { FA_BWD_PRE = 1, FA_BWD_MAIN = 2, FA_BWD_CAST = 4, FA_BWD_ALL = 7 };
 FA_API fa_status fa_backward_stages(const fa_dims* dims, const void* Q, const void* K, const void* V, const void* O,
                                     const void* dO, const float* L, void* dQ, void* dK, void* dV, void* workspace,
                                     size_t workspace_bytes, int stages, void* stream);
+
+/* Backward pass for callers that cannot allocate device memory, such as code
+ * running inside a host framework that passes it only its inputs and outputs
+ * and owns every other byte of device memory, or a latency-critical loop that
+ * must not call cudaMalloc.  Same arguments and results as fa_backward, but
+ * no workspace: the scratch comes from a fixed array of
+ * FA_NOALLOC_SCRATCH_BYTES that the library keeps in device memory on every
+ * GPU that loads it, for the life of the process.  This entry point has no
+ * counterpart on the pages; it is an interface convenience.
+ *  - A problem whose fa_backward_workspace_bytes exceeds
+ *    FA_NOALLOC_SCRATCH_BYTES is rejected with FA_ERR_SCRATCH_TOO_SMALL
+ *    before anything is enqueued (use fa_backward for it).
+ *  - Nothing is allocated or freed.  The first call on each device looks up
+ *    the array's device address with that device current; make that first
+ *    call before any stream capture on the device.
+ *  - All calls on a device share the array.  Calls that may overlap on the
+ *    GPU race on it; the caller must order them (e.g. one stream).  Stale
+ *    contents from an earlier call are harmless: every part of the scratch the
+ *    backward reads is rewritten (the dQ accumulator is zeroed) first. */
+#define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
+FA_API fa_status fa_backward_noalloc(const fa_dims* dims, const void* Q, const void* K, const void* V,
+                                     const void* O, const void* dO, const float* L, void* dQ, void* dK, void* dV,
+                                     void* stream);
 
 /* Static description of a status code. */
 FA_API const char* fa_status_string(fa_status s);

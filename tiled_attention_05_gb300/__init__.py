@@ -26,7 +26,9 @@ from . import build as _build
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 
 EXPORTED_SYMBOLS = ("fa_forward", "fa_backward", "fa_backward_stages", "fa_backward_workspace_bytes",
-                    "fa_status_string", "fa_last_device_status", "fa_last_launch_count")
+                    "fa_backward_noalloc", "fa_status_string", "fa_last_device_status", "fa_last_launch_count")
+FA_ERR_SCRATCH_TOO_SMALL = 5
+FA_NOALLOC_SCRATCH_BYTES = 32 << 20
 FA_BWD_PRE, FA_BWD_MAIN, FA_BWD_CAST, FA_BWD_ALL = 1, 2, 4, 7
 
 
@@ -67,6 +69,8 @@ def load(path: str | None = None):
             lib.fa_backward_stages.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
                                                ctypes.c_int, vp]
             lib.fa_backward_stages.restype = ctypes.c_int
+            lib.fa_backward_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.fa_backward_noalloc.restype = ctypes.c_int
             lib.fa_backward_workspace_bytes.argtypes = [dp]
             lib.fa_backward_workspace_bytes.restype = ctypes.c_size_t
             lib.fa_status_string.argtypes = [ctypes.c_int]
@@ -166,6 +170,29 @@ def fa_backward(Q, K, V, O, dO, L, causal: bool, scale: float | None = None, dQ=
     else:
         code = lib.fa_backward_stages(*args, int(stages), _stream_ptr(stream))
     _raise(code, "fa_backward")
+    return dQ, dK, dV
+
+
+def fa_backward_noalloc(Q, K, V, O, dO, L, causal: bool, scale: float | None = None, dQ=None, dK=None, dV=None,
+                        stream=None):
+    """fa_backward without a workspace, for callers that cannot allocate device
+    memory: the library's fixed scratch array (FA_NOALLOC_SCRATCH_BYTES per
+    GPU) is used instead.  Pass preallocated dQ / dK / dV to allocate nothing
+    at all; calls that could overlap on the GPU must be ordered by the caller."""
+    lib = load()
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (dO, "dO")):
+        _check(t, n)
+    _check(L, "L", torch.float32)
+    dims = _dims_of(Q, K, V, causal, scale)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    for t, n in ((dQ, "dQ"), (dK, "dK"), (dV, "dV")):
+        _check(t, n)
+    code = lib.fa_backward_noalloc(ctypes.byref(dims), Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                                   dO.data_ptr(), L.data_ptr(), dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(),
+                                   _stream_ptr(stream))
+    _raise(code, "fa_backward_noalloc")
     return dQ, dK, dV
 
 

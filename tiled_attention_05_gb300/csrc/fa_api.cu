@@ -183,6 +183,8 @@ const char* fa_status_string(fa_status s) {
       return "CUDA error while encoding tensor maps or launching kernels";
     case FA_ERR_TIMEOUT:
       return "a kernel gave up waiting on an on-chip barrier; outputs are undefined";
+    case FA_ERR_SCRATCH_TOO_SMALL:
+      return "problem needs more scratch than fa_backward_noalloc's fixed array holds; use fa_backward";
   }
   return "unknown status";
 }
