@@ -33,7 +33,7 @@ METRIC = "attention fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor 
 # workload, from one ncu capture (profiles/fa_bwd_main_<workload>.md).  Valid
 # only for the source it was taken on: reported as null once that changes.
 NCU_TRAFFIC = {
-    "gqa_B2_H32x8_T8192_d128_causal": {"bytes": 2379315000 + 1156660000, "source_sha256_16": "05f793c80d91fb73"},
+    "gqa_B2_H32x8_T8192_d128_causal": {"bytes": 2421436000 + 1182154000, "source_sha256_16": "049d77784b419c84"},
 }
 TRAFFIC_SOURCES = ("tiled_attention_05_gb300/csrc/fa_bwd.cu", "tiled_attention_05_gb300/csrc/sm103_ptx.cuh")
 

@@ -33,11 +33,11 @@
 //               w owns query columns [64w, 64w+64)): P = exp2(S*scale*log2e - L2)
 //               with masks -> TMEM; dS = P * (dP - D) -> shared memory.
 //               Epilogue: dV and dK*scale -> bf16 -> TMA store.
-//   warps 12..15 dQ warpgroup (thread = query row): copies dQ_t out of TMEM in
-//               32-column chunks into a 128B-swizzled fp32 staging buffer
-//               (two 16 KB slots) and adds each chunk into the fp32 accumulator
-//               in global memory with one TMA bulk reduce-add.
-// dS uses the bf16-rounded P that also feeds the dV MMA.
+//   warps 12..15 dQ warpgroup (thread = query row): each warp copies its 32
+//               rows of dQ_t out of TMEM two 32-column chunks at a time into its
+//               own 128B-swizzled fp32 staging slots and adds each chunk into
+//               the fp32 accumulator in global memory with one TMA bulk
+//               reduce-add (32 x 32 box); no cross-warp synchronisation.
 // TMEM columns: S^T/P [0,128), dP^T/dQ [128,256), dV [256,256+d), dK [256+d, 256+2d).
 #include <cstdint>
 
@@ -56,14 +56,14 @@ template <int HD>
 struct BwdCfg {
   static constexpr int TILE = 128 * HD * 2;  // one Q, dO, K or V tile (bf16)
   static constexpr int DS_BYTES = BN * BM * 2;
-  static constexpr int STG_SLOT = 128 * 32 * 4;  // 128 rows x 32 fp32 columns
+  static constexpr int STG_SLOT = 32 * 32 * 4;  // one warp's 32 rows x 32 fp32 columns
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
   static constexpr int OFF_Q = OFF_V + TILE;       // [2]
   static constexpr int OFF_DO = OFF_Q + 2 * TILE;  // [1]
   static constexpr int OFF_DS = OFF_DO + TILE;
-  static constexpr int OFF_STG = OFF_DS + DS_BYTES;    // [2] dQ staging slots
-  static constexpr int OFF_LSE = OFF_STG + 2 * STG_SLOT;  // [2][128] fp32
+  static constexpr int OFF_STG = OFF_DS + DS_BYTES;       // [4 warps][2] dQ staging slots
+  static constexpr int OFF_LSE = OFF_STG + 8 * STG_SLOT;  // [2][128] fp32
   static constexpr int OFF_DELTA = OFF_LSE + 2 * 512;  // [2][128] fp32
   static constexpr int OFF_BAR = OFF_DELTA + 2 * 512;
   static constexpr int NBAR = 24;
@@ -103,8 +103,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_empty = bars + 13;
   uint64_t* acc_done = bars + 14;
   uint64_t* drain = bars + 15;
-  uint64_t* stg_full = bars + 16;  // [2]
-  uint64_t* stg_free = bars + 18;  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -128,8 +126,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
-      mbar_init(&stg_full[s], 128);
-      mbar_init(&stg_free[s], 1);
     }
     mbar_init(do_full, 1);
     mbar_init(do_empty, 1);
@@ -272,28 +268,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // ---- P = exp2(S * scale * log2e - L2), masked; 32 query columns at a time.
       // The packed bf16 P of chunk c is stored over S columns this thread has
-      // already read (each thread only touches its own TMEM lane).
+      // already read (each thread only touches its own TMEM lane); the fp32 P
+      // stays in registers for dS.
       const bool need_mask = !key_valid || (CAUSAL && k0 + BN - 1 > q0 + p.causal_off);
       // key row `key` is visible to query q0 + c iff key <= q0 + c + off
       const int vis_from = key_valid ? (CAUSAL ? key - p.causal_off - q0 : -0x40000000) : 0x40000000;
-      uint32_t pk[32];  // P as packed bf16 pairs, query columns wg*64 .. wg*64+63
+      const float4* lse4 = reinterpret_cast<const float4*>(lse_s + wg * 64);
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      float pr[64];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t sr[32];
         tmem_ld32(T_S + lane_base + wg * 64 + ch * 32, sr);
         tmem_wait_ld();
+        uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int qc = wg * 64 + ch * 32 + c;
-          float v0 = ex2(fmaf(__uint_as_float(sr[c]), sl2, -lse_s[qc]));
-          float v1 = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, -lse_s[qc + 1]));
+        for (int c = 0; c < 32; c += 4) {
+          const float4 l4 = ld_shared_f4(lse4 + ((ch * 32 + c) >> 2));  // 16-byte broadcast: 4 columns
+          const uint64_t x01 = f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2,
+                                      f2_pack(-l4.x, -l4.y));
+          const uint64_t x23 = f2_fma(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), sl2x2,
+                                      f2_pack(-l4.z, -l4.w));
+          float v0 = ex2(f2_lo(x01)), v1 = ex2(f2_hi(x01)), v2 = ex2(f2_lo(x23)), v3 = ex2(f2_hi(x23));
           if (need_mask) {
+            const int qc = wg * 64 + ch * 32 + c;
             if (qc < vis_from) v0 = 0.f;
             if (qc + 1 < vis_from) v1 = 0.f;
+            if (qc + 2 < vis_from) v2 = 0.f;
+            if (qc + 3 < vis_from) v3 = 0.f;
           }
-          pk[ch * 16 + c / 2] = pack_bf16x2(v0, v1);
+          pr[ch * 32 + c] = v0;
+          pr[ch * 32 + c + 1] = v1;
+          pr[ch * 32 + c + 2] = v2;
+          pr[ch * 32 + c + 3] = v3;
+          pk[c / 2] = pack_bf16x2(v0, v1);
+          pk[c / 2 + 1] = pack_bf16x2(v2, v3);
         }
-        tmem_st16(T_S + lane_base + wg * 64 + ch * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[ch * 16]));
+        tmem_st16(T_S + lane_base + wg * 64 + ch * 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -304,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the dK / dQ MMAs of the previous tile must be done reading dS
       if (t > 0 && !mbar_wait(dq_full, (t - 1) & 1, abort_flag)) { ok = false; break; }
       uint8_t* ds_blk = smem + C::OFF_DS + wg * (BN * 128);
+      const float4* del4 = reinterpret_cast<const float4*>(del_s + wg * 64);
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t dr[32];
@@ -313,14 +325,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = cc * 8 + 2 * e;           // column inside the chunk
-            const int qc = wg * 64 + ch * 32 + c;   // query column inside the tile
-            const uint32_t pp = pk[ch * 16 + c / 2];
-            const float p0 = __uint_as_float(pp << 16), p1 = __uint_as_float(pp & 0xffff0000u);
-            const float d0 = p0 * (__uint_as_float(dr[c]) - del_s[qc]);
-            const float d1 = p1 * (__uint_as_float(dr[c + 1]) - del_s[qc + 1]);
-            w[e] = pack_bf16x2(d0, d1);
+          for (int e = 0; e < 4; e += 2) {
+            const int c = cc * 8 + 2 * e;  // column inside the chunk (4 per step)
+            const float4 d4 = ld_shared_f4(del4 + ((ch * 32 + c) >> 2));
+            const uint64_t g01 = f2_sub(f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), f2_pack(d4.x, d4.y));
+            const uint64_t g23 = f2_sub(f2_pack(__uint_as_float(dr[c + 2]), __uint_as_float(dr[c + 3])), f2_pack(d4.z, d4.w));
+            const uint64_t s01 = f2_mul(g01, f2_pack(pr[ch * 32 + c], pr[ch * 32 + c + 1]));
+            const uint64_t s23 = f2_mul(g23, f2_pack(pr[ch * 32 + c + 2], pr[ch * 32 + c + 3]));
+            w[e] = pack_bf16x2(f2_lo(s01), f2_hi(s01));
+            w[e + 1] = pack_bf16x2(f2_lo(s23), f2_hi(s23));
           }
           st_shared_v4(smem_u32(ds_blk + sw128_offset(r, ch * 4 + cc)), w[0], w[1], w[2], w[3]);
         }
@@ -381,56 +394,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ warpgroup
+    // Each warp drains its own 32 query rows (its TMEM lanes): two 4 KB
+    // staging slots per warp (32 rows x 32 fp32, 128B-swizzled), one 32x32
+    // TMA reduce-add per slot; only warp-local ordering is needed.
     const int quad = warp & 3;
-    const int r = quad * 32 + lane;  // TMEM lane = query row of the tile
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const bool leader = (warp == 12 && lane == 0);
+    const bool leader = (lane == 0);
+    uint8_t* wslot = smem + C::OFF_STG + quad * (2 * C::STG_SLOT);
     constexpr int NCH = HD / 32;  // 32-column chunks per tile, drained two at a time
     bool ok = run;
-    int k = 0;  // chunks staged so far; chunk k uses slot k & 1
-    // Stage one 32-column chunk (already in registers) into its slot and let the
-    // leader add it into the accumulator.  A slot is reused two chunks later;
-    // the leader confirms that the copy out of it has been read only then, so
-    // the bulk read overlaps the next chunk.
-    auto stage = [&](const uint32_t (&v)[32], int col, int row0, int bh) -> bool {
-      const int slot = k & 1;
-      if (k >= 2) {
-        if (leader) {
-          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // chunk k-2 read
-          mbar_arrive(&stg_free[slot]);
-        }
-        if (!mbar_wait(&stg_free[slot], ((k >> 1) - 1) & 1, abort_flag)) return false;
-      }
-      uint8_t* stg = smem + C::OFF_STG + slot * C::STG_SLOT;
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st_shared_v4(smem_u32(stg + sw128_offset(r, q)), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      fence_async_smem();
-      mbar_arrive(&stg_full[slot]);
-      if (leader) {
-        if (!mbar_wait(&stg_full[slot], (k >> 1) & 1, abort_flag)) return false;
-        tma_reduce_add_3d(&tmAcc, stg, col, row0, bh);
-        bulk_commit();
-      }
-      ++k;
-      return true;
-    };
     for (int t = 0; ok && t < T; ++t) {
       const int g = t / n_m, m = m_begin + (t - g * n_m);
       const int bh = b * p.Hq + hk * p.G + g;
       if (!mbar_wait(dq_full, t & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      for (int c = 0; ok && c < NCH; c += 2) {
+#pragma unroll
+      for (int c = 0; c < NCH; c += 2) {
         uint32_t v0[32], v1[32];
         tmem_ld32(T_DP + lane_base + c * 32, v0);
-        if (c + 1 < NCH) tmem_ld32(T_DP + lane_base + (c + 1) * 32, v1);
+        tmem_ld32(T_DP + lane_base + (c + 1) * 32, v1);
         tmem_wait_ld();
         if (c + 2 >= NCH) {
           tc_fence_before();
           mbar_arrive(dq_empty);  // all of dQ_t is out of TMEM: it may take dP_{t+1}
         }
-        if (!stage(v0, c * 32, m * BM, bh)) { ok = false; break; }
-        if (c + 1 < NCH && !stage(v1, (c + 1) * 32, m * BM, bh)) { ok = false; break; }
+        if (leader) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // both slots read
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          st_shared_v4(smem_u32(wslot + sw128_offset(lane, q)), v0[4 * q], v0[4 * q + 1], v0[4 * q + 2],
+                       v0[4 * q + 3]);
+          st_shared_v4(smem_u32(wslot + C::STG_SLOT + sw128_offset(lane, q)), v1[4 * q], v1[4 * q + 1],
+                       v1[4 * q + 2], v1[4 * q + 3]);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (leader) {
+          tma_reduce_add_3d(&tmAcc, wslot, c * 32, m * BM + quad * 32, bh);
+          tma_reduce_add_3d(&tmAcc, wslot + C::STG_SLOT, (c + 1) * 32, m * BM + quad * 32, bh);
+          bulk_commit();
+        }
       }
     }
     if (leader) bulk_wait0();  // every reduce-add has landed before the kernel ends
@@ -610,7 +613,7 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
       !encode_rows_bf16(&maps[3], dO, pr.d, pr.Tq, (long long)pr.B * pr.Hq) ||
       !encode_rows_bf16(&maps[4], dK, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
       !encode_rows_bf16(&maps[5], dV, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
-      !encode_acc_f32(&maps[6], dq_acc, pr.d, pr.Tq_pad(), (long long)pr.B * pr.Hq))
+      !encode_acc_f32(&maps[6], dq_acc, pr.d, pr.Tq_pad(), (long long)pr.B * pr.Hq, 32))
     return cudaErrorInvalidValue;
   BwdParams bp;
   bp.lse2 = lse2;

@@ -258,28 +258,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN; ++c)
           if (c >= lim) sr[c] = __float_as_uint(NEG_INF);
       }
-      float mt = __uint_as_float(sr[0]);
+      // row max: eight independent three-input max chains (short dependency depth)
+      float pm[8];
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mt = fmaxf(mt, __uint_as_float(sr[c]));
+      for (int k = 0; k < 8; ++k) pm[k] = __uint_as_float(sr[k]);
+#pragma unroll
+      for (int c = 8; c < BN; c += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pm[k] = fmax3(pm[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+      const float mt = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
       const float mt2 = mt * sl2;
       float m_new = m_ref;
       if (mt2 > m_ref + kRescaleThreshold) m_new = mt2;  // also taken when m_ref == -inf
       const float base = (m_new == NEG_INF) ? 0.f : m_new;
-      // exponentials; P (packed bf16 pairs) goes over the already-loaded scores
-      // in TMEM 16 columns at a time, so few registers hold it
-      float rowsum = 0.f;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nbase2 = f2_pack(-base, -base);
+      // exponentials (argument and row sum on packed pairs); P (packed bf16)
+      // goes over the already-loaded scores in TMEM 16 columns at a time
+      uint64_t rs[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float e0 = ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e]), sl2, -base));
-          const float e1 = ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e + 1]), sl2, -base));
-          rowsum += e0 + e1;
+          const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[32 * c + 2 * e]), __uint_as_float(sr[32 * c + 2 * e + 1])),
+                                    sl2x2, nbase2);
+          const float e0 = ex2(f2_lo(x)), e1 = ex2(f2_hi(x));
+          rs[e & 3] = f2_add(rs[e & 3], f2_pack(e0, e1));
           pk[e] = pack_bf16x2(e0, e1);
         }
         tmem_st16(tS + 16 * c, pk);
       }
+      const uint64_t rs2 = f2_add(f2_add(rs[0], rs[1]), f2_add(rs[2], rs[3]));
+      const float rowsum = f2_lo(rs2) + f2_hi(rs2);
       // O_X is idle here: the P.V of tile j-1 completed before S_X(j) did.
       if (m_new != m_ref) {
         const float alpha = (m_ref == NEG_INF) ? 0.f : ex2(m_ref - m_new);

@@ -25,8 +25,8 @@ struct Problem {
 bool encode_rows_bf16(CUtensorMap* map, const void* base, int inner, int rows, long long outer);
 
 // TMA descriptor for the fp32 dQ accumulator viewed as [outer][rows][inner]
-// (inner = d), box = 32 x 128 x 1 (128 bytes x 128 rows), 128-byte swizzle.
-bool encode_acc_f32(CUtensorMap* map, const void* base, int inner, long long rows, long long outer);
+// (inner = d), box = 32 x box_rows x 1 (128 bytes x box_rows), 128-byte swizzle.
+bool encode_acc_f32(CUtensorMap* map, const void* base, int inner, long long rows, long long outer, int box_rows);
 
 // Device status word of the current device (see fa_last_device_status).
 int* device_status_word();
