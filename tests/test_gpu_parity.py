@@ -9,6 +9,7 @@ complete) of the backward.
 """
 from __future__ import annotations
 
+import json
 import math
 
 import numpy as np
@@ -164,22 +165,29 @@ def test_workload_full_size(fa, name):
     # forward: sampled rows of the first and last head of the first and last batch
     heads = sorted({(0, 0), (0, w.Hq - 1), (w.B - 1, w.Hq // 2), (w.B - 1, w.Hq - 1)})
     rows = sample_rows(w.Tq)
+    fwd_err = {"O": {"max_abs": 0.0, "max_abs_beyond_rounding": 0.0, "rel_l2": 0.0}, "L": {"max_abs": 0.0}}
     for b, h in heads:
         kvh = h // G
         Qh, Kh, Vh = (oracle._f64(t) for t in (Q[b:b + 1, h:h + 1], K[b:b + 1, kvh:kvh + 1],
                                                  V[b:b + 1, kvh:kvh + 1]))
         for r in rows:
             O, L = oracle.forward(Qh, Kh, Vh, w.causal, rows=(r, r + 1))
-            assert_close(f"O[{b},{h},{r}]", got["O"][b, h, r], O[0, 0, r])
-            assert_L_close(f"L[{b},{h},{r}]", got["L"][b, h, r:r + 1], L[0, 0, r:r + 1])
+            eo = assert_close(f"O[{b},{h},{r}]", got["O"][b, h, r], O[0, 0, r])
+            el = assert_L_close(f"L[{b},{h},{r}]", got["L"][b, h, r:r + 1], L[0, 0, r:r + 1])
+            for k in ("max_abs", "max_abs_beyond_rounding", "rel_l2"):
+                fwd_err["O"][k] = max(fwd_err["O"][k], eo[k])
+            fwd_err["L"]["max_abs"] = max(fwd_err["L"]["max_abs"], el["max_abs"])
     # backward: one complete GQA group (the last one: last batch, last kv head).
     b, kvh = w.B - 1, w.Hkv - 1
     hs = slice(kvh * G, (kvh + 1) * G)
     dQ, dK, dV, _ = oracle.backward(Q[b:b + 1, hs], K[b:b + 1, kvh:kvh + 1], V[b:b + 1, kvh:kvh + 1],
                                     dO[b:b + 1, hs], w.causal)
-    assert_close("dQ(group)", got["dQ"][b:b + 1, hs], dQ)
-    assert_close("dK(group)", got["dK"][b:b + 1, kvh:kvh + 1], dK)
-    assert_close("dV(group)", got["dV"][b:b + 1, kvh:kvh + 1], dV)
+    report = {"workload": name}
+    report["dQ"] = assert_close("dQ(group)", got["dQ"][b:b + 1, hs], dQ)
+    report["dK"] = assert_close("dK(group)", got["dK"][b:b + 1, kvh:kvh + 1], dK)
+    report["dV"] = assert_close("dV(group)", got["dV"][b:b + 1, kvh:kvh + 1], dV)
+    report["O"], report["L"] = fwd_err["O"], fwd_err["L"]
+    print("PARITY", json.dumps(report))
     # the whole output is finite
     for n in ("O", "L", "dQ", "dK", "dV"):
         assert torch.isfinite(got[n].float()).all(), n

@@ -26,12 +26,13 @@
 //                 S^T  = K Q_t^T        -> TMEM [0,128)      (key rows = lanes)
 //                 dP^T = V dO_t^T       -> TMEM [128,256)
 //                 dV  += P^T dO_t       A = P^T from TMEM (bf16, written over S^T)
-//                 dK  += dS^T Q_t       A = dS^T from shared memory (K-major)
+//                 dK  += dS^T Q_t       A = dS^T from TMEM (bf16, the other half of S^T)
 //                 dQ_t = dS K           -> TMEM [128,128+d)  A = the same dS bytes
 //                                        read MN-major; B = K read MN-major
 //   warps 4..11 two elementwise warpgroups (thread = key row = TMEM lane; group
 //               w owns query columns [64w, 64w+64)): P = exp2(S*scale*log2e - L2)
-//               with masks -> TMEM; dS = P * (dP - D) -> shared memory.
+//               with masks -> TMEM; dS = P * (dP - D) -> shared memory (for the
+//               dQ MMA) and, packed, into TMEM (for the dK MMA).
 //               Epilogue: dV and dK*scale -> bf16 -> TMA store.
 //   warps 12..15 dQ warpgroup (thread = query row): each warp copies its 32
 //               rows of dQ_t out of TMEM two 32-column chunks at a time into its
@@ -228,14 +229,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < BM / 16; ++k)
           mma_ts(T_DV, T_S + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(do_base + k * 2048, BM * 128), id_kv,
                  (t > 0 || k > 0) ? 1u : 0u);
-        mma_commit(tS_free);
         mma_commit(do_empty);
         if (!mbar_wait(ds_ready, t & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
+        // dS^T lives in TMEM too, packed into the other half of each group's
+        // S^T columns: query columns [0,64) at [32,64), [64,128) at [96,128).
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
-          mma_ss(T_DK, desc_kmajor(ds_base + (k >> 2) * (BN * 128) + (k & 3) * 32),
-                 desc_mnmajor(q_base + k * 2048, BM * 128), id_kv, (t > 0 || k > 0) ? 1u : 0u);
+          mma_ts(T_DK, T_S + (k >> 2) * 64 + 32 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_kv,
+                 (t > 0 || k > 0) ? 1u : 0u);
+        mma_commit(tS_free);  // P^T and dS^T (both in the S^T columns) consumed
         mma_commit(&q_empty[st]);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
@@ -336,8 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             w[e + 1] = pack_bf16x2(f2_lo(s23), f2_hi(s23));
           }
           st_shared_v4(smem_u32(ds_blk + sw128_offset(r, ch * 4 + cc)), w[0], w[1], w[2], w[3]);
+          // packed dS^T of these 8 columns, for the dK MMA (A from TMEM)
+          tmem_st4(T_S + lane_base + wg * 64 + 32 + ch * 16 + cc * 4, w[0], w[1], w[2], w[3]);
         }
       }
+      tmem_wait_st();
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(ds_ready);

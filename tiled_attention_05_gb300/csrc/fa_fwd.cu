@@ -27,6 +27,7 @@
 // TMEM columns: S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,256+d), O_B [384,384+d).
 // Scores are kept in log2 units (scale * log2(e) folded into one FMA).
 #include <cstdint>
+#include <cstdlib>
 
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
@@ -61,6 +62,7 @@ struct FwdParams {
   int causal_off;  // Tk - Tq
   int kv_tiles;
   float scale_log2;  // scale * log2(e)
+  int test_withhold_q;  // failure-path test only: never issue the Q load (every wait then times out)
 };
 
 // Key tiles that query rows [qa, qa+128) must visit.
@@ -135,11 +137,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_BYTES);
+      if (!p.test_withhold_q) {
+        mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_BYTES);
 #pragma unroll
-      for (int cb = 0; cb < HD / 64; ++cb) {
-        tma_load_3d(smem + C::OFF_Q + cb * BM * 128, &tmQ, q_full, cb * 64, q0, bh);
-        if (has_b) tma_load_3d(smem + C::OFF_Q + C::Q_BYTES + cb * BM * 128, &tmQ, q_full, cb * 64, q0 + BM, bh);
+        for (int cb = 0; cb < HD / 64; ++cb) {
+          tma_load_3d(smem + C::OFF_Q + cb * BM * 128, &tmQ, q_full, cb * 64, q0, bh);
+          if (has_b) tma_load_3d(smem + C::OFF_Q + C::Q_BYTES + cb * BM * 128, &tmQ, q_full, cb * 64, q0 + BM, bh);
+        }
       }
       int k_last[NS], v_last[NS];
 #pragma unroll
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         v_last[s] = u;
       }
       // Every issued copy must land before the CTA releases its shared memory.
-      mbar_wait_bounded(q_full, 0);
+      if (!p.test_withhold_q) mbar_wait_bounded(q_full, 0);
 #pragma unroll
       for (int s = 0; s < NS; ++s) {
         if (k_last[s] >= 0) mbar_wait_bounded(&k_full[s], k_last[s] & 1);
@@ -385,6 +389,11 @@ cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUt
   p.causal_off = pr.Tk - pr.Tq;
   p.kv_tiles = pr.kv_tiles();
   p.scale_log2 = pr.scale * 1.4426950408889634f;
+  // Failure-path test switch (FA_TEST_WITHHOLD_Q=1): the producer withholds
+  // the Q tile, so the CTA's bounded waits expire and the kernel reports
+  // FA_ERR_TIMEOUT through the device status word instead of hanging.
+  const char* wq = getenv("FA_TEST_WITHHOLD_Q");
+  p.test_withhold_q = (wq && wq[0] == '1') ? 1 : 0;
   dim3 grid(pr.B * pr.Hq, (pr.q_tiles() + 1) / 2);
   fa_fwd_kernel<HD, CAUSAL><<<grid, kThreads, C::SMEM, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
