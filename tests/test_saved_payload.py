@@ -1,0 +1,148 @@
+"""Saved-for-backward payload of four attention strategies, measured with the
+instrument of "What Ordinary Autograd Saves" (section "Looking at what
+autograd keeps"): a saved_tensors_hooks pack hook that counts each stashed
+tensor's bytes once per (storage, offset, shape, stride, dtype).
+
+Strategies (section "The measurement" and "The way out is recomputation"):
+  * dense        -- softmax(Q K^T / sqrt(d)) V under autograd;
+  * tiled        -- the online-softmax tiled forward under ordinary autograd;
+  * checkpointed -- the tiled forward wrapped in torch.utils.checkpoint;
+  * this library -- the keep-O-and-L custom backward (GPU test).
+
+What is pinned: the dense and checkpointed payloads equal their closed forms
+(Q+K+V plus one T x T softmax output; Q+K+V) -- the page's table agrees with
+those exactly -- and the tiled payload behaves as the page reports: quadratic
+(growth toward 4x per doubling of T), larger than dense, and made only of
+tile-sized tensors.  The page notes that the tiled path's exact integers depend
+on the PyTorch version; on the versions named in the test (the page's 2.8 and
+the ones this build runs) they reproduce the printed table exactly and are
+checked against tests/golden/p1_saved_payload.txt.  This library's own payload
+(Q, K, V, O and L only) is checked on the GPU in test_gpu_parity.py.
+"""
+import math
+import os
+
+import pytest
+import torch
+from torch.utils.checkpoint import checkpoint
+
+import oracle
+
+
+class Payload:
+    def __init__(self):
+        self.seen, self.bytes, self.events, self.largest = set(), 0, 0, 0
+
+    def pack(self, t):
+        self.events += 1
+        self.largest = max(self.largest, t.numel())
+        key = (t.untyped_storage().data_ptr(), t.storage_offset(), tuple(t.shape), tuple(t.stride()), t.dtype)
+        if key not in self.seen:
+            self.seen.add(key)
+            self.bytes += t.numel() * t.element_size()
+        return t.detach()
+
+
+def payload_of(fn, *args):
+    p = Payload()
+    with torch.autograd.graph.saved_tensors_hooks(p.pack, lambda t: t):
+        out = fn(*args)
+        (out[0] if isinstance(out, tuple) else out).sum().backward()
+    return p
+
+
+def tiled_forward(Q, K, V, bq=32, bk=32):
+    """Online-softmax tiled forward in plain torch ops (float32): running max,
+    sum and unnormalised output per row, one rescale when the max moves."""
+    Tq, d = Q.shape
+    Tk, dv = K.shape[0], V.shape[1]
+    scale = 1.0 / math.sqrt(d)
+    outs, lses = [], []
+    for i in range(0, Tq, bq):
+        q = Q[i:i + bq]
+        m = torch.full((q.shape[0],), -torch.inf)
+        l = torch.zeros(q.shape[0])
+        acc = torch.zeros(q.shape[0], dv)
+        for j in range(0, Tk, bk):
+            S = (q @ K[j:j + bk].T) * scale
+            m_new = torch.maximum(m, S.max(dim=-1).values)
+            alpha = torch.where(torch.isneginf(m), torch.zeros_like(m), torch.exp(m - m_new))
+            P = torch.exp(S - m_new[:, None])
+            l = l * alpha + P.sum(dim=-1)
+            acc = acc * alpha[:, None] + P @ V[j:j + bk]
+            m = m_new
+        outs.append(acc / l[:, None])
+        lses.append(m + torch.log(l))
+    return torch.cat(outs), torch.cat(lses)
+
+
+def dense(Q, K, V):
+    return torch.softmax((Q @ K.T) / math.sqrt(Q.shape[-1]), -1) @ V
+
+
+def tiled_checkpointed(Q, K, V):
+    return checkpoint(lambda q, k, v: tiled_forward(q, k, v)[0], Q, K, V, use_reentrant=False)
+
+
+def measure(T, d=32):
+    torch.manual_seed(0)
+    Q, K, V = (torch.randn(T, d, requires_grad=True) for _ in range(3))
+    res = {}
+    for name, fn in (("tiled", tiled_forward), ("dense", dense), ("checkpointed", tiled_checkpointed)):
+        for t in (Q, K, V):
+            t.grad = None
+        res[name] = payload_of(fn, Q, K, V)
+    return res
+
+
+def test_payload_table_shapes_and_closed_forms():
+    torch.set_num_threads(1)
+    prev = None
+    rows = []
+    for T in (128, 256, 512, 1024):
+        r = measure(T)
+        d = 32
+        assert r["dense"].bytes == oracle.saved_bytes("dense", 1, 1, 1, T, T, d, d, elem_bytes=4, prob_bytes=4)
+        assert r["checkpointed"].bytes == oracle.saved_bytes("checkpoint", 1, 1, 1, T, T, d, d, elem_bytes=4)
+        # tiled: larger than dense, never a tensor bigger than one 32 x 32 tile
+        assert r["tiled"].bytes > r["dense"].bytes
+        assert r["tiled"].largest == 32 * 32
+        if prev is not None:
+            growth = r["tiled"].bytes / prev
+            assert 3.0 < growth < 4.2  # quadratic: toward 4x per doubling
+        prev = r["tiled"].bytes
+        rows.append((T, r["tiled"].bytes // 1024, r["dense"].bytes // 1024, r["checkpointed"].bytes // 1024,
+                     r["tiled"].events))
+    print("\nT  tiled_KiB  dense_KiB  checkpointed_KiB  tiled_save_events")
+    for row in rows:
+        print(*row)
+    # On the PyTorch versions the page was measured on (2.8) and this build is
+    # tested with, the tiled column reproduces the printed table exactly.
+    if tuple(int(x) for x in torch.__version__.split(".")[:2]) in {(2, 8), (2, 9), (2, 10), (2, 11)}:
+        golden = {}
+        for line in open(os.path.join(os.path.dirname(__file__), "golden", "p1_saved_payload.txt")):
+            if line.startswith("#") or not line.strip() or line.startswith("T "):
+                continue
+            T, tiled_kib, dense_kib, events, largest = (int(x) for x in line.split())
+            golden[T] = (tiled_kib, dense_kib, events, largest)
+        for T, tiled_kib, dense_kib, _, events in rows:
+            assert (tiled_kib, dense_kib, events) == golden[T][:3], (T, golden[T])
+    # recomputation shrinks the payload by ~4x at T = 128 and ~25x at T = 1024
+    assert 3 < rows[0][1] / rows[0][3] < 6 and 20 < rows[3][1] / rows[3][3] < 32
+
+
+def test_tiled_and_checkpointed_gradients_equal_dense():
+    """The page's equivalence check (random cotangent, float32)."""
+    torch.manual_seed(2)
+    T, d = 128, 32
+    Q, K, V = (torch.randn(T, d, requires_grad=True) for _ in range(3))
+    up = torch.randn(T, d)
+    grads = {}
+    for name, fn in (("dense", dense), ("ckpt", tiled_checkpointed), ("tiled", lambda q, k, v: tiled_forward(q, k, v)[0])):
+        for t in (Q, K, V):
+            t.grad = None
+        (fn(Q, K, V) * up).sum().backward()
+        grads[name] = [t.grad.clone() for t in (Q, K, V)]
+    for other in ("ckpt", "tiled"):
+        for g, r in zip(grads[other], grads["dense"]):
+            torch.testing.assert_close(g, r, atol=1e-5, rtol=1e-5)
