@@ -84,9 +84,9 @@ class OracleLib:
         lib = ctypes.CDLL(path)
         dp = ctypes.POINTER(ctypes.c_double)
         i = ctypes.c_int
-        lib.fa_oracle_forward.argtypes = [dp, dp, dp, i, i, i, i, i, i, i, i, ctypes.c_double, i, i, dp, dp, i]
+        lib.fa_oracle_forward.argtypes = [dp, dp, dp, i, i, i, i, i, i, i, i, i, ctypes.c_double, i, i, dp, dp, i]
         lib.fa_oracle_forward.restype = None
-        lib.fa_oracle_backward.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, i, i, ctypes.c_double,
+        lib.fa_oracle_backward.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, i, i, i, ctypes.c_double,
                                            dp, dp, dp, dp, i]
         lib.fa_oracle_backward.restype = None
         lib.fa_oracle_saved_bytes.argtypes = [i] * 11
@@ -95,10 +95,11 @@ class OracleLib:
         self.path = path
 
     def forward(self, Q, K, V, causal: bool, scale: float | None = None, rows: tuple[int, int] | None = None,
-                nthreads: int = 0):
+                nthreads: int = 0, window: int = 0):
         """Return (O, L) as float64 numpy arrays [B,Hq,Tq,dv] / [B,Hq,Tq].
 
         ``rows=(lo, hi)`` computes only query rows lo..hi-1 of every head (others are NaN).
+        ``window=W`` (causal only) limits each row to its last W keys; 0 = no limit.
         """
         Q, K, V = _f64(Q), _f64(K), _f64(V)
         B, Hq, Hkv, Tq, Tk, d, dv = _dims(Q, K, V)
@@ -106,11 +107,11 @@ class OracleLib:
         lo, hi = rows if rows is not None else (0, Tq)
         O = np.full((B, Hq, Tq, dv), np.nan)
         L = np.full((B, Hq, Tq), np.nan)
-        self.lib.fa_oracle_forward(_ptr(Q), _ptr(K), _ptr(V), B, Hq, Hkv, Tq, Tk, d, dv, int(bool(causal)), scale,
-                                   int(lo), int(hi), _ptr(O), _ptr(L), int(nthreads))
+        self.lib.fa_oracle_forward(_ptr(Q), _ptr(K), _ptr(V), B, Hq, Hkv, Tq, Tk, d, dv, int(bool(causal)),
+                                   int(window), scale, int(lo), int(hi), _ptr(O), _ptr(L), int(nthreads))
         return O, L
 
-    def backward(self, Q, K, V, dO, causal: bool, scale: float | None = None, nthreads: int = 0):
+    def backward(self, Q, K, V, dO, causal: bool, scale: float | None = None, nthreads: int = 0, window: int = 0):
         """Return (dQ, dK, dV, D) as float64 numpy arrays for the loss <O, dO>."""
         Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
         B, Hq, Hkv, Tq, Tk, d, dv = _dims(Q, K, V)
@@ -122,7 +123,8 @@ class OracleLib:
         dV = np.empty((B, Hkv, Tk, dv))
         D = np.zeros((B, Hq, Tq))
         self.lib.fa_oracle_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), B, Hq, Hkv, Tq, Tk, d, dv,
-                                    int(bool(causal)), scale, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(D), int(nthreads))
+                                    int(bool(causal)), int(window), scale, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(D),
+                                    int(nthreads))
         return dQ, dK, dV, D
 
     def saved_bytes(self, strategy: str, B, Hq, Hkv, Tq, Tk, d, dv, elem_bytes, stat_bytes=4,

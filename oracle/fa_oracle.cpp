@@ -22,8 +22,12 @@
 //                                      tiled forward returns as `mi + log(li)`)
 //
 // Visible keys: j < Tk, and with causal masking j <= i + (Tk - Tq)
-// (bottom-right alignment; identical to top-left when Tq == Tk).  A row with
-// no visible key gets O_i = 0, L_i = -inf and no gradient.
+// (bottom-right alignment; identical to top-left when Tq == Tk).  With a
+// sliding window of W >= 1 keys (causal only; the local-attention layers of
+// "The Autograd Memory Trap", section "Assumptions and Uncertainties", item 3,
+// which see a bounded number of keys), also j > i + (Tk - Tq) - W: the row sees
+// at most its last W keys.  A row with no visible key gets O_i = 0,
+// L_i = -inf and no gradient.
 //
 // Backward, derived by hand from the softmax Jacobian dp_j/ds_k = p_j(d_jk - p_k)
 // for a loss with upstream gradient dO (no equations survive on the pages;
@@ -49,7 +53,7 @@
 namespace {
 
 struct Dims {
-  int B, Hq, Hkv, Tq, Tk, d, dv, causal;
+  int B, Hq, Hkv, Tq, Tk, d, dv, causal, window;
   double scale;
 };
 
@@ -62,16 +66,27 @@ inline int64_t visible_end(const Dims& z, int64_t i) {
   return e;
 }
 
-// Scores, probabilities and logsumexp of one query row.  Returns the number of
-// visible keys n; p[0..n) is filled, *lse set (-inf when n == 0).
-int64_t row_probs(const Dims& z, const double* q, const double* Kh, int64_t i, double* p, double* lse) {
+// First visible key index for query row i (0 unless a sliding window is set).
+inline int64_t visible_begin(const Dims& z, int64_t i) {
+  if (!z.causal || z.window <= 0) return 0;
+  int64_t b = i + (int64_t)(z.Tk - z.Tq) - z.window + 1;
+  return b < 0 ? 0 : b;
+}
+
+// Scores, probabilities and logsumexp of one query row.  Visible keys are
+// [j0, n); returns n with p[j0..n) filled, *j0 set, *lse set (-inf when the
+// range is empty).
+int64_t row_probs(const Dims& z, const double* q, const double* Kh, int64_t i, double* p, double* lse,
+                  int64_t* j0) {
   const int64_t n = visible_end(z, i);
-  if (n == 0) {
+  *j0 = visible_begin(z, i);
+  if (*j0 >= n) {
     *lse = -std::numeric_limits<double>::infinity();
-    return 0;
+    *j0 = n;
+    return n;
   }
   double m = -std::numeric_limits<double>::infinity();
-  for (int64_t j = 0; j < n; ++j) {
+  for (int64_t j = *j0; j < n; ++j) {
     const double* k = Kh + j * z.d;
     double s = 0.0;
     for (int c = 0; c < z.d; ++c) s += q[c] * k[c];
@@ -80,11 +95,11 @@ int64_t row_probs(const Dims& z, const double* q, const double* Kh, int64_t i, d
     if (s > m) m = s;
   }
   double l = 0.0;
-  for (int64_t j = 0; j < n; ++j) {
+  for (int64_t j = *j0; j < n; ++j) {
     p[j] = std::exp(p[j] - m);
     l += p[j];
   }
-  for (int64_t j = 0; j < n; ++j) p[j] /= l;
+  for (int64_t j = *j0; j < n; ++j) p[j] /= l;
   *lse = m + std::log(l);
   return n;
 }
@@ -96,9 +111,9 @@ extern "C" {
 // Forward on rows [row_lo, row_hi) of every (b, h); other rows of O and L are
 // left untouched.  nthreads <= 0 uses the OpenMP default.
 void fa_oracle_forward(const double* Q, const double* K, const double* V, int B, int Hq, int Hkv, int Tq, int Tk,
-                       int d, int dv, int causal, double scale, int row_lo, int row_hi, double* O, double* L,
-                       int nthreads) {
-  const Dims z{B, Hq, Hkv, Tq, Tk, d, dv, causal, scale};
+                       int d, int dv, int causal, int window, double scale, int row_lo, int row_hi, double* O,
+                       double* L, int nthreads) {
+  const Dims z{B, Hq, Hkv, Tq, Tk, d, dv, causal, window, scale};
   const int G = Hq / Hkv;
   if (row_lo < 0) row_lo = 0;
   if (row_hi > Tq) row_hi = Tq;
@@ -121,9 +136,10 @@ void fa_oracle_forward(const double* Q, const double* K, const double* V, int B,
       const double* Vh = V + (b * Hkv + kvh) * (int64_t)Tk * dv;
       double* o = O + ((b * Hq + h) * (int64_t)Tq + i) * dv;
       double lse;
-      const int64_t n = row_probs(z, q, Kh, i, p.data(), &lse);
+      int64_t j0;
+      const int64_t n = row_probs(z, q, Kh, i, p.data(), &lse, &j0);
       for (int c = 0; c < dv; ++c) o[c] = 0.0;
-      for (int64_t j = 0; j < n; ++j) {
+      for (int64_t j = j0; j < n; ++j) {
         const double* v = Vh + j * dv;
         for (int c = 0; c < dv; ++c) o[c] += p[j] * v[c];
       }
@@ -135,9 +151,9 @@ void fa_oracle_forward(const double* Q, const double* K, const double* V, int B,
 // Full backward for every (b, h).  dQ [B,Hq,Tq,d], dK [B,Hkv,Tk,d],
 // dV [B,Hkv,Tk,dv] are overwritten.  D_out (nullable) receives D_i.
 void fa_oracle_backward(const double* Q, const double* K, const double* V, const double* dO, int B, int Hq, int Hkv,
-                        int Tq, int Tk, int d, int dv, int causal, double scale, double* dQ, double* dK, double* dV,
-                        double* D_out, int nthreads) {
-  const Dims z{B, Hq, Hkv, Tq, Tk, d, dv, causal, scale};
+                        int Tq, int Tk, int d, int dv, int causal, int window, double scale, double* dQ, double* dK,
+                        double* dV, double* D_out, int nthreads) {
+  const Dims z{B, Hq, Hkv, Tq, Tk, d, dv, causal, window, scale};
   const int G = Hq / Hkv;
 #ifdef _OPENMP
   if (nthreads > 0) omp_set_num_threads(nthreads);
@@ -170,9 +186,10 @@ void fa_oracle_backward(const double* Q, const double* K, const double* V, const
         const double* q = Q + row * d;
         const double* g = dO + row * dv;
         double lse;
-        const int64_t n = row_probs(z, q, Kh, i, p.data(), &lse);
+        int64_t j0;
+        const int64_t n = row_probs(z, q, Kh, i, p.data(), &lse, &j0);
         double Di = 0.0;
-        for (int64_t j = 0; j < n; ++j) {
+        for (int64_t j = j0; j < n; ++j) {
           const double* v = Vh + j * dv;
           double s = 0.0;
           for (int c = 0; c < dv; ++c) s += g[c] * v[c];
@@ -181,7 +198,7 @@ void fa_oracle_backward(const double* Q, const double* K, const double* V, const
         }
         if (D_out) D_out[row] = Di;
         double* dq = dQ + row * d;
-        for (int64_t j = 0; j < n; ++j) {
+        for (int64_t j = j0; j < n; ++j) {
           const double dS = p[j] * (dP[j] - Di);
           const double* k = Kh + j * d;
           double* dk = dKp.data() + j * d;

@@ -74,6 +74,21 @@ def test_small_shapes_full_parity(fa, shape):
     assert_close("dV", got["dV"], dV)
 
 
+@pytest.mark.parametrize("Tq", [32, 300])
+def test_appended_queries_over_long_prefix(fa, Tq):
+    """Queries appended after an ~8000-token prefix (Tk = 8000 + 32, 32 query / 8
+    KV heads, d = 128, causal, bottom-right aligned) -- the attention shape of
+    "The Autograd Memory Trap", section "The Reasoning" -- checked in full."""
+    Q, K, V, dO = make_custom(1, 32, 8, Tq, 8032, 128, True, seed=Tq)
+    got = run_gpu(fa, Q, K, V, dO, True)
+    O, L = oracle.forward(Q, K, V, True)
+    dQ, dK, dV, _ = oracle.backward(Q, K, V, dO, True)
+    assert_close("O", got["O"], O)
+    assert_L_close("L", got["L"], L)
+    for n, ref in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+        assert_close(n, got[n], ref)
+
+
 def test_explicit_scale(fa):
     Q, K, V, dO = make_custom(1, 2, 1, 200, 260, 128, False, seed=7)
     got = run_gpu(fa, Q, K, V, dO, False, scale=0.05)

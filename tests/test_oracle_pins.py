@@ -47,20 +47,23 @@ def make(B, Hq, Hkv, Tq, Tk, d, dv=None, seed=0):
             rnd((B, Hq, Tq, dv), seed + 3))
 
 
-def visible_mask(Tq, Tk, causal):
+def visible_mask(Tq, Tk, causal, window=0):
     i = torch.arange(Tq)[:, None]
     j = torch.arange(Tk)[None, :]
     if not causal:
         return torch.ones(Tq, Tk, dtype=torch.bool)
-    return j <= i + (Tk - Tq)
+    m = j <= i + (Tk - Tq)
+    if window > 0:
+        m = m & (j > i + (Tk - Tq) - window)
+    return m
 
 
-def torch_reference(Q, K, V, dO, causal, scale):
+def torch_reference(Q, K, V, dO, causal, scale, window=0):
     """torch float64 SDPA (GQA by repeat_interleave) + autograd; returns O, L, dQ, dK, dV."""
     Qt, Kt, Vt = (torch.tensor(a, requires_grad=True) for a in (Q, K, V))
     G = Q.shape[1] // K.shape[1]
     Ke, Ve = Kt.repeat_interleave(G, dim=1), Vt.repeat_interleave(G, dim=1)
-    mask = visible_mask(Q.shape[2], K.shape[2], causal)
+    mask = visible_mask(Q.shape[2], K.shape[2], causal, window)
     O = F.scaled_dot_product_attention(Qt, Ke, Ve, attn_mask=mask, scale=scale)
     S = (Qt @ Ke.transpose(-1, -2)) * scale
     L = torch.logsumexp(S.masked_fill(~mask, -math.inf), dim=-1)
@@ -84,9 +87,9 @@ def rel(a, b):
     return float(np.max(np.abs(a - b)) / max(1e-3, np.max(np.abs(b))))
 
 
-def fd_grads(lib, Q, K, V, dO, causal, scale, h=1e-6):
+def fd_grads(lib, Q, K, V, dO, causal, scale, h=1e-6, window=0):
     def loss(Q_, K_, V_):
-        O, _ = lib.forward(Q_, K_, V_, causal, scale)
+        O, _ = lib.forward(Q_, K_, V_, causal, scale, window=window)
         return float(np.sum(O * dO))
 
     grads = []
@@ -158,6 +161,15 @@ def pin_suite(lib, quick=False):
             failed.append(f"D-identity:{n}")
         if not np.allclose(dK.sum(axis=2), 0.0, atol=1e-12):
             failed.append(f"sum-dK:{n}")
+    # sliding window against the band-masked library reference
+    for n, (Tq, Tk, W) in enumerate(((23, 23, 5), (9, 30, 7))):
+        Q, K, V, dO = make(1, 4, 2, Tq, Tk, 8, seed=200 + n)
+        O, L = lib.forward(Q, K, V, True, 0.4, window=W)
+        dQ, dK, dV, _ = lib.backward(Q, K, V, dO, True, 0.4, window=W)
+        ref = torch_reference(Q, K, V, dO, True, 0.4, window=W)
+        for name, a, b in zip(("O", "L", "dQ", "dK", "dV"), (O, L, dQ, dK, dV), ref):
+            if not np.all(np.isfinite(a)) or rel(a, b) > 1e-11:
+                failed.append(f"window:{name}:{n}")
     # finite differences on a tiny causal GQA problem
     Q, K, V, dO = make(1, 2, 1, 7, 7, 4, seed=99)
     for causal in (True, False):
@@ -331,6 +343,51 @@ def test_thread_count_does_not_change_results(oracle_lib):
         assert np.allclose(x, y, rtol=1e-14, atol=1e-15)
 
 
+@pytest.mark.parametrize("Tq,Tk,W", [(40, 40, 1), (40, 40, 7), (33, 70, 16), (70, 33, 5), (64, 64, 200)])
+def test_sliding_window_matches_torch_float64(oracle_lib, Tq, Tk, W):
+    Q, K, V, dO = make(2, 4, 2, Tq, Tk, 8, seed=Tq + W)
+    O, L = oracle_lib.forward(Q, K, V, True, 0.45, window=W)
+    dQ, dK, dV, _ = oracle_lib.backward(Q, K, V, dO, True, 0.45, window=W)
+    vis = visible_mask(Tq, Tk, True, W)
+    if bool(vis.any(dim=1).all()):
+        Or, Lr, dQr, dKr, dVr = torch_reference(Q, K, V, dO, True, 0.45, window=W)
+        assert rel(O, Or) < 1e-12 and rel(L, Lr) < 1e-12
+        assert rel(dQ, dQr) < 1e-11 and rel(dK, dKr) < 1e-11 and rel(dV, dVr) < 1e-11
+    # rows without a visible key follow the empty-row policy
+    empty = ~vis.any(dim=1).numpy()
+    assert np.all(O[:, :, empty] == 0) and np.all(np.isneginf(L[:, :, empty]))
+
+
+def test_window_wider_than_keys_is_plain_causal(oracle_lib):
+    Q, K, V, dO = make(1, 2, 1, 30, 45, 8, seed=21)
+    a = oracle_lib.forward(Q, K, V, True, 0.3)
+    b = oracle_lib.forward(Q, K, V, True, 0.3, window=45)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+    ga = oracle_lib.backward(Q, K, V, dO, True, 0.3)
+    gb = oracle_lib.backward(Q, K, V, dO, True, 0.3, window=1000)
+    # (the backward's per-thread partial sums are added in a run-dependent order)
+    assert all(np.allclose(x, y, rtol=0, atol=1e-14) for x, y in zip(ga, gb))
+
+
+def test_window_of_one_sees_only_the_diagonal(oracle_lib):
+    Tq, Tk = 12, 20
+    off = Tk - Tq
+    Q, K, V, dO = make(1, 1, 1, Tq, Tk, 4, seed=22)
+    O, L = oracle_lib.forward(Q, K, V, True, 0.5, window=1)
+    assert np.allclose(O[0, 0], V[0, 0, off:], atol=1e-15)
+    assert np.allclose(L[0, 0], 0.5 * np.sum(Q[0, 0] * K[0, 0, off:], axis=-1), atol=1e-14)
+    dQ, dK, dV, _ = oracle_lib.backward(Q, K, V, dO, True, 0.5, window=1)
+    assert np.max(np.abs(dQ)) < 1e-15 and np.max(np.abs(dK)) < 1e-15
+    assert np.allclose(dV[0, 0, off:], dO[0, 0], atol=1e-15) and np.all(dV[0, 0, :off] == 0)
+
+
+def test_window_backward_matches_finite_differences(oracle_lib):
+    Q, K, V, dO = make(1, 2, 1, 9, 9, 4, seed=23)
+    dQ, dK, dV, _ = oracle_lib.backward(Q, K, V, dO, True, 0.6, window=3)
+    fQ, fK, fV = fd_grads(oracle_lib, Q, K, V, dO, True, 0.6, window=3)
+    assert rel(dQ, fQ) < 1e-7 and rel(dK, fK) < 1e-7 and rel(dV, fV) < 1e-7
+
+
 # ----------------------------------------------------------------- saved payload (golden)
 def read_golden(name):
     rows = []
@@ -394,6 +451,7 @@ MUTANTS = {
     "lse-max-dropped": ("*lse = m + std::log(l);", "*lse = std::log(l);"),
     "dP-wrong-operand": ("s += g[c] * v[c];", "s += g[c] * Kh[j * z.d + c];"),
     "dQ-uses-q": ("dq[c] += scale * dS * k[c];", "dq[c] += scale * dS * q[c];"),
+    "window-off-by-one": ("- z.window + 1;", "- z.window;"),
 }
 
 
