@@ -175,7 +175,7 @@ def oracle_sample(w, rows: int | None, group: int = 0):
     if w.causal and w.Tq != w.Tk and rows is not None:
         Tk = w.Tk - (w.Tq - Tq)
     Q, K, V, dO = make_custom(1, G, 1, Tq, Tk, w.d, w.causal, seed=w.seed + 1000 * group, dO_std=w.dO_std)
-    sw = Workload("sample", 1, G, 1, Tq, Tk, w.d, w.causal, w.seed)
+    sw = Workload("sample", 1, G, 1, Tq, Tk, w.d, w.causal, w.seed, window=w.window)
     return (Q, K, V, dO), sw
 
 
@@ -185,8 +185,8 @@ def time_oracle(w, rows, nthreads, group: int = 0):
     (Q, K, V, dO), sw = oracle_sample(w, rows, group)
     Qn, Kn, Vn, dOn = (oracle._f64(t) for t in (Q, K, V, dO))
     t0 = time.perf_counter()
-    oracle.forward(Qn, Kn, Vn, w.causal, nthreads=nthreads)
-    oracle.backward(Qn, Kn, Vn, dOn, w.causal, nthreads=nthreads)
+    oracle.forward(Qn, Kn, Vn, w.causal, nthreads=nthreads, window=w.window)
+    oracle.backward(Qn, Kn, Vn, dOn, w.causal, nthreads=nthreads, window=w.window)
     dt = time.perf_counter() - t0
     return sw.flops("fwdbwd"), dt, sw
 
@@ -227,12 +227,12 @@ def run_reference(args, w):
             secs += dt
     value = flops_sum / secs / 1e12
     sample = (f"one GQA group (batch 0, kv head 0, {w.G} query heads), Tq={sw.Tq}, Tk={sw.Tk}, d={w.d}, "
-              f"causal={w.causal}; float64 forward + backward")
+              f"causal={w.causal}, window={w.window}; float64 forward + backward")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Tq": w.Tq, "Tk": w.Tk, "d": w.d,
-                       "causal": w.causal},
+                       "causal": w.causal, "window": w.window},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -264,7 +264,7 @@ def run_ours(args, w):
     O = torch.empty_like(Q)
     L = torch.empty(w.B, w.Hq, w.Tq, dtype=torch.float32, device=dev)
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
-    dims = fa.make_dims(w.B, w.Hq, w.Hkv, w.Tq, w.Tk, w.d, w.dv, w.causal, None)
+    dims = fa.make_dims(w.B, w.Hq, w.Hkv, w.Tq, w.Tk, w.d, w.dv, w.causal, None, w.window)
     ws = torch.empty(fa.fa_backward_workspace_bytes(dims), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -273,19 +273,19 @@ def run_ours(args, w):
         launches = 0
         if evs:
             evs[0].record(stream)
-        fa.fa_forward(Q, K, V, w.causal, None, O=O, L=L)
+        fa.fa_forward(Q, K, V, w.causal, None, O=O, L=L, window=w.window)
         launches += fa.last_launch_count()
         if evs:
             evs[1].record(stream)
-        fa.fa_backward(Q, K, V, O, dO, L, w.causal, None, dQ, dK, dV, ws, stages=fa.FA_BWD_PRE)
+        fa.fa_backward(Q, K, V, O, dO, L, w.causal, None, dQ, dK, dV, ws, stages=fa.FA_BWD_PRE, window=w.window)
         launches += fa.last_launch_count()
         if evs:
             evs[2].record(stream)
-        fa.fa_backward(Q, K, V, O, dO, L, w.causal, None, dQ, dK, dV, ws, stages=fa.FA_BWD_MAIN)
+        fa.fa_backward(Q, K, V, O, dO, L, w.causal, None, dQ, dK, dV, ws, stages=fa.FA_BWD_MAIN, window=w.window)
         launches += fa.last_launch_count()
         if evs:
             evs[3].record(stream)
-        fa.fa_backward(Q, K, V, O, dO, L, w.causal, None, dQ, dK, dV, ws, stages=fa.FA_BWD_CAST)
+        fa.fa_backward(Q, K, V, O, dO, L, w.causal, None, dQ, dK, dV, ws, stages=fa.FA_BWD_CAST, window=w.window)
         launches += fa.last_launch_count()
         if evs:
             evs[4].record(stream)
@@ -363,8 +363,9 @@ def run_ours(args, w):
             if k >= 2:
                 stream.wait_event(st_["read"])  # step k-2's results have been read back
             q, kk, v, g = st_["in"]
-            fa.fa_forward(q, kk, v, w.causal, None, O=st_["O"], L=st_["L"], stream=stream)
-            fa.fa_backward(q, kk, v, st_["O"], g, st_["L"], w.causal, None, *st_["res"], st_["ws"], stream=stream)
+            fa.fa_forward(q, kk, v, w.causal, None, O=st_["O"], L=st_["L"], stream=stream, window=w.window)
+            fa.fa_backward(q, kk, v, st_["O"], g, st_["L"], w.causal, None, *st_["res"], st_["ws"], stream=stream,
+                           window=w.window)
             st_["computed"].record(stream)
             with torch.cuda.stream(s_down):
                 s_down.wait_event(st_["computed"])
@@ -399,7 +400,7 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Tq": w.Tq, "Tk": w.Tk, "d": w.d,
-                       "causal": w.causal, "parallelism": "replicas" if world > 1 else "single",
+                       "causal": w.causal, "window": w.window, "parallelism": "replicas" if world > 1 else "single",
                        "l2": "flushed before every timed step (256 MiB write)"},
             "pct_of_peak": 100.0 * value / peak,
             "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,

@@ -27,8 +27,12 @@
  *
  * Masking: key j is visible to query i iff j < Tk and, when causal, also
  * j <= i + (Tk - Tq) (bottom-right alignment, the same as top-left when
- * Tq == Tk).  A query row that sees no key gets O = 0, L = -inf, dQ = 0 and
- * contributes nothing to dK, dV.
+ * Tq == Tk).  A causal sliding window of W >= 1 keys (the local-attention
+ * layers of "The Autograd Memory Trap", section "Assumptions and
+ * Uncertainties", item 3, which attend to a bounded number of keys) further
+ * requires j > i + (Tk - Tq) - W: each row sees at most its last W keys.
+ * A query row that sees no key gets O = 0, L = -inf, dQ = 0 and contributes
+ * nothing to dK, dV.
  *
  * Supported: d == dv in {64, 128}.  Any B, Hq, Hkv, Tq, Tk >= 0 (ragged tails
  * are handled; a zero-sized problem is a no-op; Tk == 0 yields O = 0 and
@@ -75,6 +79,7 @@ typedef struct {
   int B, Hq, Hkv, Tq, Tk, d, dv;
   int causal; /* 0 or 1 */
   float scale; /* multiplies Q K^T; <= 0 selects 1/sqrt(d) */
+  int window;  /* causal sliding window in keys; 0 = none; > 0 needs causal == 1 */
 } fa_dims;
 
 /* Forward pass: O = softmax(scale * Q K^T + mask) V, L = logsumexp rows.

@@ -39,10 +39,10 @@ def test_status_strings():
 
 
 def dims(**kw):
-    base = dict(B=1, Hq=4, Hkv=2, Tq=100, Tk=90, d=128, dv=128, causal=0, scale=0.0)
+    base = dict(B=1, Hq=4, Hkv=2, Tq=100, Tk=90, d=128, dv=128, causal=0, scale=0.0, window=0)
     base.update(kw)
     return fa.FaDims(base["B"], base["Hq"], base["Hkv"], base["Tq"], base["Tk"], base["d"], base["dv"],
-                     base["causal"], base["scale"])
+                     base["causal"], base["scale"], base["window"])
 
 
 def call_fwd(d, ptrs=(0x1000, 0x2000, 0x3000, 0x4000, 0x5000)):
@@ -56,6 +56,8 @@ def call_fwd(d, ptrs=(0x1000, 0x2000, 0x3000, 0x4000, 0x5000)):
     dict(B=-1),
     dict(Tq=-5),
     dict(causal=2),
+    dict(window=64),         # a window needs the causal mask
+    dict(causal=1, window=-1),
     dict(scale=float("nan")),
     dict(scale=float("inf")),
 ])

@@ -1,8 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
 
 Small shapes are compared element by element in full (several 128-row tiles,
-ragged tails, GQA, causal with Tq == Tk, Tq < Tk and Tq > Tk, empty rows).
-The five named workloads run at full size in the same launch configuration
+ragged tails, GQA, causal with Tq == Tk, Tq < Tk and Tq > Tk, empty rows,
+causal sliding windows).  The named workloads run at full size in the same launch configuration
 the benchmark times; the oracle checks sampled forward rows of several heads
 and one complete GQA group (all of its query heads and rows, so dK and dV are
 complete) of the backward.
@@ -33,13 +33,13 @@ def fa():
     return lib
 
 
-def run_gpu(fa, Q, K, V, dO, causal, scale=None, backward=True):
+def run_gpu(fa, Q, K, V, dO, causal, scale=None, backward=True, window=0):
     dev = torch.device("cuda")
     Qd, Kd, Vd, dOd = (t.to(dev) for t in (Q, K, V, dO))
-    O, L = fa.fa_forward(Qd, Kd, Vd, causal, scale)
+    O, L = fa.fa_forward(Qd, Kd, Vd, causal, scale, window=window)
     out = {"O": O, "L": L}
     if backward:
-        dQ, dK, dV = fa.fa_backward(Qd, Kd, Vd, O, dOd, L, causal, scale)
+        dQ, dK, dV = fa.fa_backward(Qd, Kd, Vd, O, dOd, L, causal, scale, window=window)
         out.update(dQ=dQ, dK=dK, dV=dV)
     torch.cuda.synchronize()
     assert fa.fa_last_device_status() == 0
@@ -87,6 +87,67 @@ def test_appended_queries_over_long_prefix(fa, Tq):
     assert_L_close("L", got["L"], L)
     for n, ref in (("dQ", dQ), ("dK", dK), ("dV", dV)):
         assert_close(n, got[n], ref)
+
+
+WINDOWED = [
+    # B, Hq, Hkv, Tq, Tk, d, window   (always causal)
+    (1, 4, 2, 700, 700, 128, 200),     # window between one and two tiles, ragged tail
+    (1, 2, 1, 513, 513, 64, 1),        # each row sees only its diagonal key
+    (1, 2, 2, 300, 800, 128, 128),     # Tq < Tk, window of exactly one tile
+    (1, 2, 1, 600, 257, 128, 100),     # Tq > Tk: empty first rows, then windows
+    (2, 4, 1, 1000, 1000, 128, 333),   # GQA 4:1, window start off the tile grid
+    (1, 4, 4, 384, 384, 64, 129),      # tile multiples, window one past a tile
+    (1, 2, 1, 300, 300, 128, 5000),    # window longer than Tk: plain causal
+]
+
+
+@pytest.mark.parametrize("shape", WINDOWED, ids=lambda s: "x".join(map(str, s[:6])) + f"w{s[6]}")
+def test_sliding_window_full_parity(fa, shape):
+    """Causal sliding-window attention (the local-attention layers of "The
+    Autograd Memory Trap", section "Assumptions and Uncertainties", item 3)
+    against the oracle's windowed mask, every element."""
+    B, Hq, Hkv, Tq, Tk, d, W = shape
+    Q, K, V, dO = make_custom(B, Hq, Hkv, Tq, Tk, d, True, seed=sum(shape))
+    got = run_gpu(fa, Q, K, V, dO, True, window=W)
+    O, L = oracle.forward(Q, K, V, True, window=W)
+    dQ, dK, dV, _ = oracle.backward(Q, K, V, dO, True, window=W)
+    assert_close("O", got["O"], O)
+    assert_L_close("L", got["L"], L)
+    for n, ref in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+        assert_close(n, got[n], ref)
+
+
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 300)])
+def test_rescale_on_some_rows_of_a_warp(fa, causal, window):
+    """Every other query row gets a component along one direction u that only
+    the keys of one later tile share, so the running maximum of those rows
+    jumps by about 2^10 (log2 units) mid-walk while their neighbours' does not:
+    the lazy O rescale is taken by some rows of a warp and not by others.
+    u = 9 * (random signs) / sqrt(d) adds 81 to those dot products while every
+    entry stays O(1)."""
+    Q, K, V, dO = make_custom(1, 2, 1, 256, 640, 128, causal, seed=41)
+    g = torch.Generator().manual_seed(5)
+    u = (torch.randint(0, 2, (128,), generator=g) * 2 - 1).float() * (9.0 / math.sqrt(128))
+    Q = Q.float()
+    K = K.float()
+    Q[:, :, 0::2] += u
+    K[:, :, 384:512] += u
+    Q, K = Q.to(torch.bfloat16), K.to(torch.bfloat16)
+    got = run_gpu(fa, Q, K, V, dO, causal, window=window)
+    O, L = oracle.forward(Q, K, V, causal, window=window)
+    dQ, dK, dV, _ = oracle.backward(Q, K, V, dO, causal, window=window)
+    assert_close("O", got["O"], O)
+    assert_L_close("L", got["L"], L)
+    for n, ref in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+        assert_close(n, got[n], ref)
+
+
+def test_window_requires_causal(fa):
+    dev = torch.device("cuda")
+    Q = torch.randn(1, 1, 64, 128, device=dev).to(torch.bfloat16)
+    with pytest.raises(fa.FAError) as e:
+        fa.fa_forward(Q, Q, Q, False, window=16)
+    assert e.value.code == fa.FA_ERR_INVALID_ARG
 
 
 def test_explicit_scale(fa):
@@ -175,7 +236,7 @@ def sample_rows(Tq):
 def test_workload_full_size(fa, name):
     w = WORKLOADS[name]
     Q, K, V, dO = make_inputs(w)
-    got = run_gpu(fa, Q, K, V, dO, w.causal)
+    got = run_gpu(fa, Q, K, V, dO, w.causal, window=w.window)
     G = w.G
     # forward: sampled rows of the first and last head of the first and last batch
     heads = sorted({(0, 0), (0, w.Hq - 1), (w.B - 1, w.Hq // 2), (w.B - 1, w.Hq - 1)})
@@ -186,7 +247,7 @@ def test_workload_full_size(fa, name):
         Qh, Kh, Vh = (oracle._f64(t) for t in (Q[b:b + 1, h:h + 1], K[b:b + 1, kvh:kvh + 1],
                                                  V[b:b + 1, kvh:kvh + 1]))
         for r in rows:
-            O, L = oracle.forward(Qh, Kh, Vh, w.causal, rows=(r, r + 1))
+            O, L = oracle.forward(Qh, Kh, Vh, w.causal, rows=(r, r + 1), window=w.window)
             eo = assert_close(f"O[{b},{h},{r}]", got["O"][b, h, r], O[0, 0, r])
             el = assert_L_close(f"L[{b},{h},{r}]", got["L"][b, h, r:r + 1], L[0, 0, r:r + 1])
             for k in ("max_abs", "max_abs_beyond_rounding", "rel_l2"):
@@ -196,7 +257,7 @@ def test_workload_full_size(fa, name):
     b, kvh = w.B - 1, w.Hkv - 1
     hs = slice(kvh * G, (kvh + 1) * G)
     dQ, dK, dV, _ = oracle.backward(Q[b:b + 1, hs], K[b:b + 1, kvh:kvh + 1], V[b:b + 1, kvh:kvh + 1],
-                                    dO[b:b + 1, hs], w.causal)
+                                    dO[b:b + 1, hs], w.causal, window=w.window)
     report = {"workload": name}
     report["dQ"] = assert_close("dQ(group)", got["dQ"][b:b + 1, hs], dQ)
     report["dK"] = assert_close("dK(group)", got["dK"][b:b + 1, kvh:kvh + 1], dK)

@@ -5,8 +5,8 @@ kernels of ``libfa_gb300.so``.  There is no CPU or PyTorch fallback -- if the
 library cannot be loaded, every entry point raises.
 
 Entry points mirror the C ABI:
-    fa_forward(Q, K, V, causal, scale=None)            -> (O, L)
-    fa_backward(Q, K, V, O, dO, L, causal, scale=None)  -> (dQ, dK, dV)
+    fa_forward(Q, K, V, causal, scale=None, window=0)            -> (O, L)
+    fa_backward(Q, K, V, O, dO, L, causal, scale=None, window=0)  -> (dQ, dK, dV)
     fa_backward_workspace_bytes(...), fa_status_string(code), fa_last_device_status()
 plus ``FlashAttention`` (a torch.autograd.Function that keeps only Q, K, V, O
 and L for the backward pass) and ``attention`` (its functional form).
@@ -41,7 +41,7 @@ class FAError(RuntimeError):
 class FaDims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("Tq", ctypes.c_int),
                 ("Tk", ctypes.c_int), ("d", ctypes.c_int), ("dv", ctypes.c_int), ("causal", ctypes.c_int),
-                ("scale", ctypes.c_float)]
+                ("scale", ctypes.c_float), ("window", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -90,12 +90,12 @@ def status_string(code: int) -> str:
 fa_status_string = status_string
 
 
-def make_dims(B, Hq, Hkv, Tq, Tk, d, dv, causal, scale) -> FaDims:
+def make_dims(B, Hq, Hkv, Tq, Tk, d, dv, causal, scale, window: int = 0) -> FaDims:
     return FaDims(int(B), int(Hq), int(Hkv), int(Tq), int(Tk), int(d), int(dv), int(bool(causal)),
-                  float(scale) if scale is not None else 0.0)
+                  float(scale) if scale is not None else 0.0, int(window))
 
 
-def _dims_of(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, causal, scale) -> FaDims:
+def _dims_of(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, causal, scale, window: int = 0) -> FaDims:
     if Q.dim() != 4 or K.dim() != 4 or V.dim() != 4:
         raise ValueError("Q, K, V must be [B, H, T, d]")
     B, Hq, Tq, d = Q.shape
@@ -103,7 +103,7 @@ def _dims_of(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, causal, scale) -
     Bv, Hv, Tv, dv = V.shape
     if not (B == Bk == Bv and Hkv == Hv and Tk == Tv and d == dk):
         raise ValueError(f"inconsistent shapes Q{tuple(Q.shape)} K{tuple(K.shape)} V{tuple(V.shape)}")
-    return make_dims(B, Hq, Hkv, Tq, Tk, d, dv, causal, scale)
+    return make_dims(B, Hq, Hkv, Tq, Tk, d, dv, causal, scale, window)
 
 
 def _check(t: torch.Tensor, name: str, dtype=torch.bfloat16):
@@ -125,12 +125,13 @@ def fa_backward_workspace_bytes(dims: FaDims) -> int:
     return int(load().fa_backward_workspace_bytes(ctypes.byref(dims)))
 
 
-def fa_forward(Q, K, V, causal: bool, scale: float | None = None, O=None, L=None, stream=None):
-    """O, L = attention forward.  Optional preallocated O / L are written in place."""
+def fa_forward(Q, K, V, causal: bool, scale: float | None = None, O=None, L=None, stream=None, window: int = 0):
+    """O, L = attention forward.  Optional preallocated O / L are written in place.
+    ``window=W`` (causal only) lets each row see at most its last W keys."""
     lib = load()
     for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
         _check(t, n)
-    dims = _dims_of(Q, K, V, causal, scale)
+    dims = _dims_of(Q, K, V, causal, scale, window)
     if O is None:
         O = torch.empty(dims.B, dims.Hq, dims.Tq, dims.dv, dtype=torch.bfloat16, device=Q.device)
     if L is None:
@@ -144,7 +145,7 @@ def fa_forward(Q, K, V, causal: bool, scale: float | None = None, O=None, L=None
 
 
 def fa_backward(Q, K, V, O, dO, L, causal: bool, scale: float | None = None, dQ=None, dK=None, dV=None,
-                workspace=None, stream=None, stages: int = FA_BWD_ALL):
+                workspace=None, stream=None, stages: int = FA_BWD_ALL, window: int = 0):
     """dQ, dK, dV = attention backward from the saved O and L.
 
     ``stages`` selects which of the three backward kernels to launch (see
@@ -154,7 +155,7 @@ def fa_backward(Q, K, V, O, dO, L, causal: bool, scale: float | None = None, dQ=
     for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (dO, "dO")):
         _check(t, n)
     _check(L, "L", torch.float32)
-    dims = _dims_of(Q, K, V, causal, scale)
+    dims = _dims_of(Q, K, V, causal, scale, window)
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
@@ -174,7 +175,7 @@ def fa_backward(Q, K, V, O, dO, L, causal: bool, scale: float | None = None, dQ=
 
 
 def fa_backward_noalloc(Q, K, V, O, dO, L, causal: bool, scale: float | None = None, dQ=None, dK=None, dV=None,
-                        stream=None):
+                        stream=None, window: int = 0):
     """fa_backward without a workspace, for callers that cannot allocate device
     memory: the library's fixed scratch array (FA_NOALLOC_SCRATCH_BYTES per
     GPU) is used instead.  Pass preallocated dQ / dK / dV to allocate nothing
@@ -183,7 +184,7 @@ def fa_backward_noalloc(Q, K, V, O, dO, L, causal: bool, scale: float | None = N
     for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (dO, "dO")):
         _check(t, n)
     _check(L, "L", torch.float32)
-    dims = _dims_of(Q, K, V, causal, scale)
+    dims = _dims_of(Q, K, V, causal, scale, window)
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
@@ -208,18 +209,18 @@ class FlashAttention(torch.autograd.Function):
     """Autograd wrapper: saves Q, K, V (inputs) plus O and L -- nothing quadratic."""
 
     @staticmethod
-    def forward(ctx, Q, K, V, causal=False, scale=None):
-        O, L = fa_forward(Q, K, V, causal, scale)
+    def forward(ctx, Q, K, V, causal=False, scale=None, window=0):
+        O, L = fa_forward(Q, K, V, causal, scale, window=window)
         ctx.save_for_backward(Q, K, V, O, L)
-        ctx.causal, ctx.scale = causal, scale
+        ctx.causal, ctx.scale, ctx.window = causal, scale, window
         return O
 
     @staticmethod
     def backward(ctx, dO):
         Q, K, V, O, L = ctx.saved_tensors
-        dQ, dK, dV = fa_backward(Q, K, V, O, dO.contiguous(), L, ctx.causal, ctx.scale)
-        return dQ, dK, dV, None, None
+        dQ, dK, dV = fa_backward(Q, K, V, O, dO.contiguous(), L, ctx.causal, ctx.scale, window=ctx.window)
+        return dQ, dK, dV, None, None, None
 
 
-def attention(Q, K, V, causal=False, scale=None):
-    return FlashAttention.apply(Q, K, V, causal, scale)
+def attention(Q, K, V, causal=False, scale=None, window=0):
+    return FlashAttention.apply(Q, K, V, causal, scale, window)

@@ -44,6 +44,7 @@ fa_status check_dims(const fa_dims* dims, fa::Problem* pr) {
   const fa_dims& z = *dims;
   if (z.B < 0 || z.Hq < 0 || z.Hkv < 0 || z.Tq < 0 || z.Tk < 0 || z.d < 1 || z.dv < 1) return FA_ERR_INVALID_ARG;
   if (z.causal != 0 && z.causal != 1) return FA_ERR_INVALID_ARG;
+  if (z.window < 0 || (z.window > 0 && !z.causal)) return FA_ERR_INVALID_ARG;
   if (z.Hq > 0 && (z.Hkv < 1 || z.Hq % z.Hkv != 0)) return FA_ERR_INVALID_ARG;
   if (!(z.scale == z.scale) || std::isinf(z.scale)) return FA_ERR_INVALID_ARG;
   if (z.dv != z.d || (z.d != 64 && z.d != 128)) return FA_ERR_UNSUPPORTED;
@@ -57,6 +58,9 @@ fa_status check_dims(const fa_dims* dims, fa::Problem* pr) {
   pr->Tk = z.Tk;
   pr->d = z.d;
   pr->causal = z.causal;
+  // A window of Tk keys or more hides nothing (row i's window starts at or
+  // before key i + Tk - Tq - Tk < 0); dropping it keeps kernel indices small.
+  pr->window = z.window >= z.Tk ? 0 : z.window;
   pr->scale = z.scale > 0.f ? z.scale : 1.0f / std::sqrt((float)z.d);
   return FA_OK;
 }
@@ -176,7 +180,7 @@ const char* fa_status_string(fa_status s) {
       return "ok";
     case FA_ERR_INVALID_ARG:
       return "invalid argument (null or misaligned pointer, negative size, Hq not a multiple of Hkv, "
-             "bad causal flag or scale, or workspace too small)";
+             "bad causal flag, window or scale, or workspace too small)";
     case FA_ERR_UNSUPPORTED:
       return "unsupported shape (d must equal dv and be 64 or 128)";
     case FA_ERR_CUDA:

@@ -14,9 +14,11 @@
 //                accumulator.  HBM-bound, one warp per row.
 //   fa_bwd_main  one CTA per (batch, kv head, 128-key tile): K and V stay in
 //                shared memory; the CTA walks the G query heads of its group
-//                and their 128-row query tiles, keeping dK and dV in TMEM for
-//                the whole walk and adding each tile's dQ into the fp32
-//                accumulator in global memory.
+//                and the 128-row query tiles that can see its keys (causal:
+//                from the diagonal on; with a sliding window of W keys, up to
+//                the last row whose window still reaches the tile), keeping dK
+//                and dV in TMEM for the whole walk and adding each tile's dQ
+//                into the fp32 accumulator in global memory.
 //   fa_dq_cast   dQ = bf16(scale * accumulator).  HBM-bound.
 //
 // fa_bwd_main roles (512 threads, four warpgroups):
@@ -77,6 +79,7 @@ struct BwdParams {
   const float* delta;
   int* status;
   int Hq, Hkv, G, Tq, Tk, causal_off, q_tiles;
+  int window;  // causal sliding window in keys, 0 = none
   long long Tq_pad;
   float scale_log2, scale;
 };
@@ -113,12 +116,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = blockIdx.y;  // key tile; causal: low tiles see the most query rows, run first
   const int k0 = n * BN;
 
-  int m_begin = 0;
+  int m_begin = 0, m_end = p.q_tiles;
   if (CAUSAL) {
     const int first_row = k0 - p.causal_off;  // first query row that sees key k0
     m_begin = first_row <= 0 ? 0 : min(p.q_tiles, first_row / BM);
+    if (p.window > 0) {
+      // last query row whose window reaches the tile's last key
+      const long long last_row = (long long)k0 + BN - 1 - p.causal_off + p.window - 1;
+      m_end = last_row < 0 ? 0 : (int)min((long long)p.q_tiles, last_row / BM + 1);
+    }
   }
-  const int n_m = p.q_tiles - m_begin;
+  const int n_m = max(0, m_end - m_begin);
   const int T = p.G * n_m;  // tiles this CTA walks
 
   if (threadIdx.x == 0) {
@@ -266,16 +274,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = m * BM;
       const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE + st * 512);
       const float* del_s = reinterpret_cast<const float*>(smem + C::OFF_DELTA + st * 512);
-      if (!mbar_wait(&q_full[st], u & 1, abort_flag)) { ok = false; break; }
-      if (!mbar_wait(s_full, t & 1, abort_flag)) { ok = false; break; }
+      // Each warp agrees on every wait's outcome before its collective TMEM
+      // loads and stores, so a timeout never splits a warp.
+      if (!__all_sync(0xffffffffu, mbar_wait(&q_full[st], u & 1, abort_flag))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full, t & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
       // ---- P = exp2(S * scale * log2e - L2), masked; 32 query columns at a time.
       // The packed bf16 P of chunk c is stored over S columns this thread has
       // already read (each thread only touches its own TMEM lane); the fp32 P
       // stays in registers for dS.
-      const bool need_mask = !key_valid || (CAUSAL && k0 + BN - 1 > q0 + p.causal_off);
-      // key row `key` is visible to query q0 + c iff key <= q0 + c + off
+      const bool win = CAUSAL && p.window > 0;
+      const bool need_mask = !key_valid || (CAUSAL && k0 + BN - 1 > q0 + p.causal_off) ||
+                             (win && q0 + BM - 1 + p.causal_off - p.window + 1 > k0);
+      // key row `key` is visible to query q0 + c iff vis_from <= c <= vis_to:
+      // key <= q0 + c + off, and with a window also key > q0 + c + off - W
       const int vis_from = key_valid ? (CAUSAL ? key - p.causal_off - q0 : -0x40000000) : 0x40000000;
+      const int vis_to = win ? key - p.causal_off - q0 + p.window - 1 : 0x40000000;
       const float4* lse4 = reinterpret_cast<const float4*>(lse_s + wg * 64);
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       float pr[64];
@@ -295,10 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v0 = ex2(f2_lo(x01)), v1 = ex2(f2_hi(x01)), v2 = ex2(f2_lo(x23)), v3 = ex2(f2_hi(x23));
           if (need_mask) {
             const int qc = wg * 64 + ch * 32 + c;
-            if (qc < vis_from) v0 = 0.f;
-            if (qc + 1 < vis_from) v1 = 0.f;
-            if (qc + 2 < vis_from) v2 = 0.f;
-            if (qc + 3 < vis_from) v3 = 0.f;
+            if (qc < vis_from || qc > vis_to) v0 = 0.f;
+            if (qc + 1 < vis_from || qc + 1 > vis_to) v1 = 0.f;
+            if (qc + 2 < vis_from || qc + 2 > vis_to) v2 = 0.f;
+            if (qc + 3 < vis_from || qc + 3 > vis_to) v3 = 0.f;
           }
           pr[ch * 32 + c] = v0;
           pr[ch * 32 + c + 1] = v1;
@@ -313,10 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(p_ready);
       // ---- dS = P * (dP - D) -> shared memory (row = key, 128B-swizzled, query-contiguous)
-      if (!mbar_wait(dp_full, t & 1, abort_flag)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(dp_full, t & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
       // the dK / dQ MMAs of the previous tile must be done reading dS
-      if (t > 0 && !mbar_wait(dq_full, (t - 1) & 1, abort_flag)) { ok = false; break; }
+      if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(dq_full, (t - 1) & 1, abort_flag))) { ok = false; break; }
       uint8_t* ds_blk = smem + C::OFF_DS + wg * (BN * 128);
       const float4* del4 = reinterpret_cast<const float4*>(del_s + wg * 64);
 #pragma unroll
@@ -350,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue: dV, dK * scale -> bf16 -> shared (the Q ring, idle now) -> TMA store
     if (ok && T > 0) {
-      if (!mbar_wait(acc_done, 0, abort_flag)) ok = false;
+      if (!__all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) ok = false;
       tc_fence_after();
     }
     const bool mine = (T == 0 || ok) && *abort_flag == 0;
@@ -412,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; ok && t < T; ++t) {
       const int g = t / n_m, m = m_begin + (t - g * n_m);
       const int bh = b * p.Hq + hk * p.G + g;
-      if (!mbar_wait(dq_full, t & 1, abort_flag)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < NCH; c += 2) {
@@ -631,6 +645,7 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
   bp.Tq = pr.Tq;
   bp.Tk = pr.Tk;
   bp.causal_off = pr.Tk - pr.Tq;
+  bp.window = pr.causal ? pr.window : 0;
   bp.q_tiles = pr.q_tiles();
   bp.Tq_pad = pr.Tq_pad();
   bp.scale = pr.scale;

@@ -26,6 +26,12 @@
 //                epilogue O / l -> bf16 -> TMA store, L -> global.
 // TMEM columns: S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,256+d), O_B [384,384+d).
 // Scores are kept in log2 units (scale * log2(e) folded into one FMA).
+//
+// Each tile visits the key tiles [beg, end) its rows can see (causal: up to
+// the diagonal; with a sliding window of W keys also from the first row's
+// window start on).  The CTA loads the union of the two ranges once; a key
+// tile inside the union that one tile does not need is skipped by that tile's
+// MMAs and softmax.
 #include <cstdint>
 #include <cstdlib>
 
@@ -60,18 +66,33 @@ struct FwdParams {
   int* status;
   int Hq, Hkv, G, Tq, Tk;
   int causal_off;  // Tk - Tq
+  int window;      // causal sliding window in keys, 0 = none
   int kv_tiles;
   float scale_log2;  // scale * log2(e)
   int test_withhold_q;  // failure-path test only: never issue the Q load (every wait then times out)
 };
 
-// Key tiles that query rows [qa, qa+128) must visit.
+// Key tiles [*beg, *end) that query rows [qa, qa+128) must visit (empty: 0, 0).
 template <bool CAUSAL>
-__device__ __forceinline__ int kv_tiles_for(const FwdParams& p, int qa) {
-  if (qa >= p.Tq) return 0;
-  if (!CAUSAL) return p.kv_tiles;
+__device__ __forceinline__ void kv_range_for(const FwdParams& p, int qa, int* beg, int* end) {
+  *beg = *end = 0;
+  if (qa >= p.Tq) return;
+  if (!CAUSAL) {
+    *end = p.kv_tiles;
+    return;
+  }
   const int last_key = min(qa + BM, p.Tq) - 1 + p.causal_off;  // last key the tile's last row sees
-  return last_key < 0 ? 0 : min(p.kv_tiles, last_key / BN + 1);
+  if (last_key < 0) return;
+  const int e = min(p.kv_tiles, last_key / BN + 1);
+  int bg = 0;
+  if (p.window > 0) {
+    const int first_key = qa + p.causal_off - p.window + 1;  // first key the tile's first row sees
+    bg = first_key > 0 ? first_key / BN : 0;
+  }
+  if (bg < e) {
+    *beg = bg;
+    *end = e;
+  }
 }
 
 template <int HD, bool CAUSAL>
@@ -100,8 +121,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / p.Hq, h = bh - b * p.Hq;
   const int q0 = (gridDim.y - 1 - blockIdx.y) * (2 * BM);  // longest causal rows first
   const int bkv = b * p.Hkv + h / p.G;
-  const int nkv_t[2] = {kv_tiles_for<CAUSAL>(p, q0), kv_tiles_for<CAUSAL>(p, q0 + BM)};
-  const int nkv_max = max(nkv_t[0], nkv_t[1]);
+  int kb[2], ke[2];  // key-tile range of tile A and tile B
+  kv_range_for<CAUSAL>(p, q0, &kb[0], &ke[0]);
+  kv_range_for<CAUSAL>(p, q0 + BM, &kb[1], &ke[1]);
+  // Union of the two ranges, loaded once.  Tile B's rows follow tile A's, so
+  // B's range starts and ends no earlier than A's, and starts no later than
+  // A's end: the union has no gap and every key tile in it is needed by A or B.
+  const int ub = ke[0] > kb[0] ? kb[0] : kb[1];
+  const int ue = max(ke[0], ke[1]);
+  const int nkv_max = ue - ub;  // key tiles the CTA loads
   const bool has_b = q0 + BM < p.Tq;
 
   if (threadIdx.x == 0) {
@@ -148,19 +176,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       int k_last[NS], v_last[NS];
 #pragma unroll
       for (int s = 0; s < NS; ++s) k_last[s] = v_last[s] = -1;
-      for (int j = 0; j < nkv_max; ++j) {
-        const int s = j % NS, u = j / NS;
+      for (int jj = 0; jj < nkv_max; ++jj) {  // ring position jj holds key tile ub + jj
+        const int s = jj % NS, u = jj / NS, kv0 = (ub + jj) * BN;
         if (!mbar_wait(&k_empty[s], (u & 1) ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(&k_full[s], C::KV_BYTES);
 #pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
-          tma_load_3d(smem + C::OFF_K + s * C::KV_BYTES + cb * BN * 128, &tmK, &k_full[s], cb * 64, j * BN, bkv);
+          tma_load_3d(smem + C::OFF_K + s * C::KV_BYTES + cb * BN * 128, &tmK, &k_full[s], cb * 64, kv0, bkv);
         k_last[s] = u;
         if (!mbar_wait(&v_empty[s], (u & 1) ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(&v_full[s], C::KV_BYTES);
 #pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
-          tma_load_3d(smem + C::OFF_V + s * C::KV_BYTES + cb * BN * 128, &tmV, &v_full[s], cb * 64, j * BN, bkv);
+          tma_load_3d(smem + C::OFF_V + s * C::KV_BYTES + cb * BN * 128, &tmV, &v_full[s], cb * 64, kv0, bkv);
         v_last[s] = u;
       }
       // Every issued copy must land before the CTA releases its shared memory.
@@ -180,10 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t v_base = smem_u32(smem + C::OFF_V);
       bool ok = mbar_wait(q_full, 0, abort_flag);
       if (ok) tc_fence_after();
+      auto active = [&](int x, int j) { return j >= kb[x] && j < ke[x]; };
       // S_X(j) = Q_X K_j^T into TMEM [128 X, 128 X + 128)
       auto issue_s = [&](int x, int j) -> bool {
-        const int s = j % NS;
-        if (!mbar_wait(&k_full[s], (j / NS) & 1, abort_flag)) return false;
+        const int s = (j - ub) % NS;
+        if (!mbar_wait(&k_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t q_base = smem_u32(smem + C::OFF_Q + x * C::Q_BYTES);
 #pragma unroll
@@ -197,32 +226,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // O_X += P_X(j) V_j with P_X read from TMEM (packed bf16 over S_X)
       auto issue_pv = [&](int x, int j) -> bool {
-        const int s = j % NS;
-        if (!mbar_wait(&p_full[x], j & 1, abort_flag)) return false;
-        if (!mbar_wait(&v_full[s], (j / NS) & 1, abort_flag)) return false;
+        const int s = (j - ub) % NS;
+        if (!mbar_wait(&p_full[x], (j - kb[x]) & 1, abort_flag)) return false;
+        if (!mbar_wait(&v_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           const uint64_t bd = desc_mnmajor(v_base + s * C::KV_BYTES + k * 2048, BN * 128);
-          mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, bd, idPV, (j > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, bd, idPV, (j > kb[x] || k > 0) ? 1u : 0u);
         }
         return true;
       };
-      if (ok && nkv_t[0] > 0) ok = issue_s(0, 0);
-      if (ok && nkv_t[1] > 0) ok = issue_s(1, 0);
+      // A tile whose range starts at ub gets its first S up front; tile B, if
+      // it starts later, gets it in the loop below one step before its range.
+      if (ok && active(0, ub)) ok = issue_s(0, ub);
+      if (ok && active(1, ub)) ok = issue_s(1, ub);
       if (ok) mma_commit(&k_empty[0]);
-      for (int j = 0; ok && j < nkv_max; ++j) {
+      for (int j = ub; ok && j < ue; ++j) {
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          if (j < nkv_t[x]) {
+          if (active(x, j)) {
             if (!issue_pv(x, j)) { ok = false; break; }
-            if (x == 1 || j >= nkv_t[1]) mma_commit(&v_empty[j % NS]);  // last reader of V_j
-            if (j + 1 < nkv_t[x]) {
-              if (!issue_s(x, j + 1)) { ok = false; break; }
-              if (x == 1 || j + 1 >= nkv_t[1]) mma_commit(&k_empty[(j + 1) % NS]);  // last reader of K_{j+1}
-            } else {
-              mma_commit(&o_done[x]);
-            }
+            if (x == 1 || !active(1, j)) mma_commit(&v_empty[(j - ub) % NS]);  // last reader of V_j
+          }
+          if (active(x, j + 1)) {
+            if (!issue_s(x, j + 1)) { ok = false; break; }
+            if (x == 1 || !active(1, j + 1)) mma_commit(&k_empty[(j + 1 - ub) % NS]);  // last reader of K_{j+1}
+          } else if (active(x, j)) {
+            mma_commit(&o_done[x]);
           }
         }
       }
@@ -233,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue of tile x
     const int x = (warp - 4) >> 2;
-    const int nkv = nkv_t[x];
+    const int kbx = x ? kb[1] : kb[0];  // first key tile of this tile's range
+    const int nkv = (x ? ke[1] : ke[0]) - kbx;
     const int qx0 = q0 + x * BM;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // row inside the tile == TMEM lane
@@ -246,21 +278,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_ref = NEG_INF;  // reference max (log2 units) the P values are taken against
     float l = 0.f;
     bool ok = run;
-    for (int j = 0; ok && j < nkv; ++j) {
-      if (!mbar_wait(&s_full[x], j & 1, abort_flag)) { ok = false; break; }
+    for (int jx = 0; ok && jx < nkv; ++jx) {  // jx-th key tile of this tile's range
+      // the warp agrees on the outcome before its collective TMEM loads
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[x], jx & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[BN];
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       tmem_wait_ld();
-      const int kv0 = j * BN;
-      const bool need_mask = (kv0 + BN > p.Tk) || (CAUSAL && kv0 + BN - 1 > qx0 + p.causal_off);
+      const int kv0 = (kbx + jx) * BN;
+      // window: the tile's last row starts its window past this key tile's start
+      const bool win_mask = CAUSAL && p.window > 0 && qx0 + BM - 1 + p.causal_off - p.window + 1 > kv0;
+      const bool need_mask = (kv0 + BN > p.Tk) || (CAUSAL && kv0 + BN - 1 > qx0 + p.causal_off) || win_mask;
       if (need_mask) {
-        int lim = p.Tk - kv0;
+        int lim = p.Tk - kv0;  // columns [lo, lim) are visible to row i
         if (CAUSAL) lim = min(lim, i + p.causal_off + 1 - kv0);
+        const int lo = win_mask ? i + p.causal_off - p.window + 1 - kv0 : -BN;
 #pragma unroll
         for (int c = 0; c < BN; ++c)
-          if (c >= lim) sr[c] = __float_as_uint(NEG_INF);
+          if (c >= lim || c < lo) sr[c] = __float_as_uint(NEG_INF);
       }
       // row max: eight independent three-input max chains (short dependency depth)
       float pm[8];
@@ -274,6 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mt2 = mt * sl2;
       float m_new = m_ref;
       if (mt2 > m_ref + kRescaleThreshold) m_new = mt2;  // also taken when m_ref == -inf
+      // Does this row's O need rescaling, and does any row of the warp's?  (The
+      // vote is taken here, where fewer registers are live than after exp2.)
+      const bool rescale = jx > 0 && m_new != m_ref && m_ref != NEG_INF;
+      const bool warp_rescale = __any_sync(0xffffffffu, rescale);
       const float base = (m_new == NEG_INF) ? 0.f : m_new;
       const uint64_t sl2x2 = f2_pack(sl2, sl2), nbase2 = f2_pack(-base, -base);
       // exponentials (argument and row sum on packed pairs); P (packed bf16)
@@ -295,30 +335,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t rs2 = f2_add(f2_add(rs[0], rs[1]), f2_add(rs[2], rs[3]));
       const float rowsum = f2_lo(rs2) + f2_hi(rs2);
       // O_X is idle here: the P.V of tile j-1 completed before S_X(j) did.
-      if (m_new != m_ref) {
-        const float alpha = (m_ref == NEG_INF) ? 0.f : ex2(m_ref - m_new);
-        l *= alpha;
-        if (j > 0 && m_ref != NEG_INF) {
+      const float alpha = (m_new == m_ref) ? 1.f : (m_ref == NEG_INF ? 0.f : ex2(m_ref - m_new));
+      l = l * alpha + rowsum;
+      // TMEM loads and stores are warp-collective: when any row of the warp
+      // must rescale its O row, every lane takes part (factor 1 where not).
+      if (warp_rescale) {
+        const float a = rescale ? alpha : 1.f;
 #pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_wait_ld();
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tO + c * 32, o);
-          }
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+          tmem_st32(tO + c * 32, o);
         }
-        m_ref = m_new;
       }
-      l += rowsum;
+      m_ref = m_new;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[x]);
     }
     // ---- epilogue: O / l -> bf16 -> shared (this tile's Q buffer, free now) -> TMA store; L -> global
     if (ok && nkv > 0) {
-      if (!mbar_wait(&o_done[x], 0, abort_flag)) ok = false;
+      if (!__all_sync(0xffffffffu, mbar_wait(&o_done[x], 0, abort_flag))) ok = false;
       tc_fence_after();
     }
     // All 128 threads of the warpgroup agree on whether to write (a timeout
@@ -387,6 +427,7 @@ cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUt
   p.Tq = pr.Tq;
   p.Tk = pr.Tk;
   p.causal_off = pr.Tk - pr.Tq;
+  p.window = pr.causal ? pr.window : 0;
   p.kv_tiles = pr.kv_tiles();
   p.scale_log2 = pr.scale * 1.4426950408889634f;
   // Failure-path test switch (FA_TEST_WITHHOLD_Q=1): the producer withholds

@@ -12,6 +12,7 @@ constexpr int kTile = 128;  // rows of a query tile and of a key/value tile
 struct Problem {
   int B, Hq, Hkv, Tq, Tk, d;
   int causal;
+  int window;   // causal sliding window in keys, 0 = none
   float scale;  // resolved (> 0)
   int G() const { return Hq / Hkv; }
   int q_tiles() const { return (Tq + kTile - 1) / kTile; }

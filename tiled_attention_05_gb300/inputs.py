@@ -28,6 +28,7 @@ class Workload:
     causal: bool
     seed: int
     dO_std: float = 1.0
+    window: int = 0  # causal sliding window in keys (0 = none)
 
     @property
     def dv(self) -> int:
@@ -38,17 +39,18 @@ class Workload:
         return self.Hq // self.Hkv
 
     def pairs_per_head(self) -> int:
-        """Unmasked (query, key) pairs of one head (bottom-right causal alignment)."""
+        """Unmasked (query, key) pairs of one head (bottom-right causal
+        alignment; with a window W, row i sees keys (i + off - W, i + off])."""
         if not self.causal:
             return self.Tq * self.Tk
-        total = 0
         off = self.Tk - self.Tq
-        # rows with at least one visible key see min(Tk, i + off + 1) keys
-        for_rows = range(self.Tq)
-        if off >= 0 and self.Tq == self.Tk:
+        if self.window <= 0 and self.Tq == self.Tk:
             return self.Tq * (self.Tq + 1) // 2
-        for i in for_rows:
-            total += max(0, min(self.Tk, i + off + 1))
+        total = 0
+        for i in range(self.Tq):
+            end = max(0, min(self.Tk, i + off + 1))
+            beg = max(0, i + off - self.window + 1) if self.window > 0 else 0
+            total += max(0, end - beg)
         return total
 
     def flops(self, part: str) -> float:
@@ -60,7 +62,10 @@ class Workload:
         return asdict(self)
 
 
-# The five workloads the library is measured and checked on.
+# The workloads the library is measured and checked on.  The last one is the
+# local-attention layer of "The Autograd Memory Trap" (section "Assumptions and
+# Uncertainties", item 3: sliding-window layers that see at most 2080 keys),
+# at the headline GQA shape.
 WORKLOADS = {
     "single_head_T256_d64": Workload("single_head_T256_d64", 1, 1, 1, 256, 256, 64, False, 1),
     "mha_B4_H16_T2048_d64_causal": Workload("mha_B4_H16_T2048_d64_causal", 4, 16, 16, 2048, 2048, 64, True, 2),
@@ -68,6 +73,8 @@ WORKLOADS = {
     "gqa_B1_H32x8_Tq4096_Tk8032_d128": Workload("gqa_B1_H32x8_Tq4096_Tk8032_d128", 1, 32, 8, 4096, 8032, 128, False,
                                                 4, dO_std=0.1),
     "long_B1_H16_T32768_d128_causal": Workload("long_B1_H16_T32768_d128_causal", 1, 16, 16, 32768, 32768, 128, True, 5),
+    "swa_B1_H32x8_T8192_W2080_d128": Workload("swa_B1_H32x8_T8192_W2080_d128", 1, 32, 8, 8192, 8192, 128, True, 6,
+                                              window=2080),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 # The workload the headline throughput is quoted on.
@@ -88,5 +95,6 @@ def make_inputs(w: Workload, seed: int | None = None):
 
 
 def make_custom(B, Hq, Hkv, Tq, Tk, d, causal, seed, dO_std=1.0):
-    """Inputs for an ad-hoc shape (edge-case tests)."""
+    """Inputs for an ad-hoc shape (edge-case tests).  The draws do not depend
+    on the mask, so a windowed case takes the same inputs as its causal one."""
     return make_inputs(Workload("custom", B, Hq, Hkv, Tq, Tk, d, causal, seed, dO_std))
