@@ -15,6 +15,7 @@ in the same metric and unit.
 from __future__ import annotations
 
 import argparse
+import atexit
 import json
 import os
 import statistics
@@ -57,7 +58,7 @@ FLUSH_BYTES = 256 << 20
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None)
@@ -105,31 +106,45 @@ def aggregate_throughput(units_per_rank: float, rank_seconds: float, world: int,
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    """Samples nvidia-smi clocks and throttle reasons every 50 ms.
+
+    It is started before the warm-up so that it is already sampling when the
+    timed region begins; each sample is stamped with the host wall clock on
+    arrival, and summary(t0, t1) keeps the samples taken inside [t0, t1].  A
+    timed region shorter than the sampling period gets the two samples around
+    it instead (both under load: warm-up before, end-to-end phase after), and
+    the summary says so."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, gpu_index: int):
         self.gpu_index = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host time of arrival, csv line)
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.PERIOD_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.reader = threading.Thread(target=self._read, daemon=True)
             self.reader.start()
         except OSError:
             self.proc = None
         return self
 
+    def wait_live(self, timeout_s: float = 3.0):
+        """Block until the first sample has arrived (or the timeout passes)."""
+        t_end = time.time() + timeout_s
+        while self.proc is not None and not self.lines and time.time() < t_end:
+            time.sleep(0.01)
+
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -140,10 +155,22 @@ class ClockSampler:
                 self.proc.kill()
             self.reader.join(timeout=2)
 
-    def summary(self):
+    def summary(self, t0: float | None = None, t1: float | None = None):
+        window = "whole run"
+        lines = self.lines
+        if t0 is not None and t1 is not None:
+            inside = [x for x in lines if t0 <= x[0] <= t1]
+            if inside:
+                lines, window = inside, "timed region"
+            else:
+                before = [x for x in lines if x[0] < t0][-1:]
+                after = [x for x in lines if x[0] > t1][:1]
+                lines = before + after
+                window = f"the samples just before and after the timed region ({(t1 - t0) * 1e3:.0f} ms, " \
+                         f"shorter than the {self.PERIOD_MS} ms sampling period)"
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for _, ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -156,8 +183,9 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0, "window": window}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "window": window}
 
 
 # ---------------------------------------------------------------- CPU oracle legs
@@ -291,6 +319,10 @@ def run_ours(args, w):
             evs[4].record(stream)
         return launches
 
+    clocks = ClockSampler(local)  # sampling from the warm-up through the end-to-end phase
+    clocks.__enter__()
+    atexit.register(clocks.__exit__, None, None, None)  # also on an error exit
+    clocks.wait_live()
     for _ in range(args.warmup):
         flush.fill_(1)
         step()
@@ -303,14 +335,14 @@ def run_ours(args, w):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
-    with clocks:
-        t_wall0 = time.perf_counter()
-        for k in range(args.steps):
-            flush.fill_(k & 0xFF)
-            launches += step(evs[k])
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
+    t_region0 = time.time()
+    t_wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        launches += step(evs[k])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    t_region1 = time.time()
     if world > 1:
         dist.barrier()
     if fa.fa_last_device_status() != fa.FA_OK:
@@ -385,6 +417,7 @@ def run_ours(args, w):
     e_end.record(s_down)
     torch.cuda.synchronize()
     e2e_secs = e_start.elapsed_time(e_end) / 1e3
+    clocks.__exit__(None, None, None)
     e2e_value, _ = aggregate_throughput(flops_step * args.steps, e2e_secs, world, backend)
 
     cpu = None
@@ -394,7 +427,7 @@ def run_ours(args, w):
     peak = peaks["bf16_tflops"]
     frac = main_tflops / peak
     if rank == 0:
-        clk = clocks.summary()
+        clk = clocks.summary(t_region0, t_region1)
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,

@@ -84,7 +84,9 @@ struct BwdParams {
   float scale_log2, scale;
 };
 
-template <int HD, bool CAUSAL>
+// WINDOW (causal only): the sliding-window terms are compiled in only where
+// a window is set, so the plain causal and full masks keep their lean code.
+template <int HD, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (CAUSAL) {
     const int first_row = k0 - p.causal_off;  // first query row that sees key k0
     m_begin = first_row <= 0 ? 0 : min(p.q_tiles, first_row / BM);
-    if (p.window > 0) {
+    if (WINDOW) {
       // last query row whose window reaches the tile's last key
       const long long last_row = (long long)k0 + BN - 1 - p.causal_off + p.window - 1;
       m_end = last_row < 0 ? 0 : (int)min((long long)p.q_tiles, last_row / BM + 1);
@@ -274,22 +276,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = m * BM;
       const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE + st * 512);
       const float* del_s = reinterpret_cast<const float*>(smem + C::OFF_DELTA + st * 512);
-      // Each warp agrees on every wait's outcome before its collective TMEM
-      // loads and stores, so a timeout never splits a warp.
-      if (!__all_sync(0xffffffffu, mbar_wait(&q_full[st], u & 1, abort_flag))) { ok = false; break; }
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full, t & 1, abort_flag))) { ok = false; break; }
+      // Each warp agrees on the outcome of the waits before its collective
+      // TMEM loads and stores, so a timeout never splits a warp.
+      bool got = mbar_wait(&q_full[st], u & 1, abort_flag) && mbar_wait(s_full, t & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after();
       // ---- P = exp2(S * scale * log2e - L2), masked; 32 query columns at a time.
       // The packed bf16 P of chunk c is stored over S columns this thread has
       // already read (each thread only touches its own TMEM lane); the fp32 P
       // stays in registers for dS.
-      const bool win = CAUSAL && p.window > 0;
       const bool need_mask = !key_valid || (CAUSAL && k0 + BN - 1 > q0 + p.causal_off) ||
-                             (win && q0 + BM - 1 + p.causal_off - p.window + 1 > k0);
+                             (WINDOW && q0 + BM - 1 + p.causal_off - p.window + 1 > k0);
       // key row `key` is visible to query q0 + c iff vis_from <= c <= vis_to:
       // key <= q0 + c + off, and with a window also key > q0 + c + off - W
       const int vis_from = key_valid ? (CAUSAL ? key - p.causal_off - q0 : -0x40000000) : 0x40000000;
-      const int vis_to = win ? key - p.causal_off - q0 + p.window - 1 : 0x40000000;
+      const int vis_to = WINDOW ? key - p.causal_off - q0 + p.window - 1 : 0x40000000;
       const float4* lse4 = reinterpret_cast<const float4*>(lse_s + wg * 64);
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       float pr[64];
@@ -309,10 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v0 = ex2(f2_lo(x01)), v1 = ex2(f2_hi(x01)), v2 = ex2(f2_lo(x23)), v3 = ex2(f2_hi(x23));
           if (need_mask) {
             const int qc = wg * 64 + ch * 32 + c;
-            if (qc < vis_from || qc > vis_to) v0 = 0.f;
-            if (qc + 1 < vis_from || qc + 1 > vis_to) v1 = 0.f;
-            if (qc + 2 < vis_from || qc + 2 > vis_to) v2 = 0.f;
-            if (qc + 3 < vis_from || qc + 3 > vis_to) v3 = 0.f;
+            if (qc < vis_from || (WINDOW && qc > vis_to)) v0 = 0.f;
+            if (qc + 1 < vis_from || (WINDOW && qc + 1 > vis_to)) v1 = 0.f;
+            if (qc + 2 < vis_from || (WINDOW && qc + 2 > vis_to)) v2 = 0.f;
+            if (qc + 3 < vis_from || (WINDOW && qc + 3 > vis_to)) v3 = 0.f;
           }
           pr[ch * 32 + c] = v0;
           pr[ch * 32 + c + 1] = v1;
@@ -327,10 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(p_ready);
       // ---- dS = P * (dP - D) -> shared memory (row = key, 128B-swizzled, query-contiguous)
-      if (!__all_sync(0xffffffffu, mbar_wait(dp_full, t & 1, abort_flag))) { ok = false; break; }
+      // dP^T is in TMEM, and the dK / dQ MMAs of the previous tile are done reading dS
+      got = mbar_wait(dp_full, t & 1, abort_flag) && (t == 0 || mbar_wait(dq_full, (t - 1) & 1, abort_flag));
+      if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after();
-      // the dK / dQ MMAs of the previous tile must be done reading dS
-      if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(dq_full, (t - 1) & 1, abort_flag))) { ok = false; break; }
       uint8_t* ds_blk = smem + C::OFF_DS + wg * (BN * 128);
       const float4* del4 = reinterpret_cast<const float4*>(del_s + wg * 64);
 #pragma unroll
@@ -541,18 +542,18 @@ __global__ void fa_zero_words(uint32_t* p, size_t n) {
   for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n; t += (size_t)gridDim.x * blockDim.x) p[t] = 0u;
 }
 
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool WINDOW>
 cudaError_t launch_main_t(const fa::Problem& pr, const CUtensorMap* maps, const BwdParams& bp, cudaStream_t stream) {
   using C = BwdCfg<HD>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(fa_bwd_main<HD, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaFuncSetAttribute(fa_bwd_main<HD, CAUSAL, WINDOW>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid(pr.B * pr.Hkv, pr.kv_tiles());
-  fa_bwd_main<HD, CAUSAL><<<grid, kThreads, C::SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+  fa_bwd_main<HD, CAUSAL, WINDOW><<<grid, kThreads, C::SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
                                                                maps[6], bp);
   return cudaGetLastError();
 }
@@ -651,9 +652,13 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
   bp.scale = pr.scale;
   bp.scale_log2 = pr.scale * 1.4426950408889634f;
   if (pr.d == 64)
-    e = pr.causal ? launch_main_t<64, true>(pr, maps, bp, stream) : launch_main_t<64, false>(pr, maps, bp, stream);
+    e = !pr.causal    ? launch_main_t<64, false, false>(pr, maps, bp, stream)
+        : pr.window ? launch_main_t<64, true, true>(pr, maps, bp, stream)
+                    : launch_main_t<64, true, false>(pr, maps, bp, stream);
   else
-    e = pr.causal ? launch_main_t<128, true>(pr, maps, bp, stream) : launch_main_t<128, false>(pr, maps, bp, stream);
+    e = !pr.causal    ? launch_main_t<128, false, false>(pr, maps, bp, stream)
+        : pr.window ? launch_main_t<128, true, true>(pr, maps, bp, stream)
+                    : launch_main_t<128, true, false>(pr, maps, bp, stream);
   if (e != cudaSuccess) return e;
   ++*launches;
   }

@@ -73,7 +73,7 @@ struct FwdParams {
 };
 
 // Key tiles [*beg, *end) that query rows [qa, qa+128) must visit (empty: 0, 0).
-template <bool CAUSAL>
+template <bool CAUSAL, bool WINDOW>
 __device__ __forceinline__ void kv_range_for(const FwdParams& p, int qa, int* beg, int* end) {
   *beg = *end = 0;
   if (qa >= p.Tq) return;
@@ -85,7 +85,7 @@ __device__ __forceinline__ void kv_range_for(const FwdParams& p, int qa, int* be
   if (last_key < 0) return;
   const int e = min(p.kv_tiles, last_key / BN + 1);
   int bg = 0;
-  if (p.window > 0) {
+  if (WINDOW) {
     const int first_key = qa + p.causal_off - p.window + 1;  // first key the tile's first row sees
     bg = first_key > 0 ? first_key / BN : 0;
   }
@@ -95,7 +95,9 @@ __device__ __forceinline__ void kv_range_for(const FwdParams& p, int qa, int* be
   }
 }
 
-template <int HD, bool CAUSAL>
+// WINDOW (causal only): the sliding-window terms are compiled in only where
+// a window is set, so the plain causal and full masks keep their lean code.
+template <int HD, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -122,8 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = (gridDim.y - 1 - blockIdx.y) * (2 * BM);  // longest causal rows first
   const int bkv = b * p.Hkv + h / p.G;
   int kb[2], ke[2];  // key-tile range of tile A and tile B
-  kv_range_for<CAUSAL>(p, q0, &kb[0], &ke[0]);
-  kv_range_for<CAUSAL>(p, q0 + BM, &kb[1], &ke[1]);
+  kv_range_for<CAUSAL, WINDOW>(p, q0, &kb[0], &ke[0]);
+  kv_range_for<CAUSAL, WINDOW>(p, q0 + BM, &kb[1], &ke[1]);
   // Union of the two ranges, loaded once.  Tile B's rows follow tile A's, so
   // B's range starts and ends no earlier than A's, and starts no later than
   // A's end: the union has no gap and every key tile in it is needed by A or B.
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       const int kv0 = (kbx + jx) * BN;
       // window: the tile's last row starts its window past this key tile's start
-      const bool win_mask = CAUSAL && p.window > 0 && qx0 + BM - 1 + p.causal_off - p.window + 1 > kv0;
+      const bool win_mask = WINDOW && qx0 + BM - 1 + p.causal_off - p.window + 1 > kv0;
       const bool need_mask = (kv0 + BN > p.Tk) || (CAUSAL && kv0 + BN - 1 > qx0 + p.causal_off) || win_mask;
       if (need_mask) {
         int lim = p.Tk - kv0;  // columns [lo, lim) are visible to row i
@@ -407,13 +409,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_flag) atomicExch(p.status, DEV_TIMEOUT);
 }
 
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool WINDOW>
 cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mo, float* L, cudaStream_t stream) {
   using C = FwdCfg<HD>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<HD, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<HD, CAUSAL, WINDOW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -436,7 +438,7 @@ cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUt
   const char* wq = getenv("FA_TEST_WITHHOLD_Q");
   p.test_withhold_q = (wq && wq[0] == '1') ? 1 : 0;
   dim3 grid(pr.B * pr.Hq, (pr.q_tiles() + 1) / 2);
-  fa_fwd_kernel<HD, CAUSAL><<<grid, kThreads, C::SMEM, stream>>>(mq, mk, mv, mo, p);
+  fa_fwd_kernel<HD, CAUSAL, WINDOW><<<grid, kThreads, C::SMEM, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 
@@ -471,11 +473,13 @@ cudaError_t launch_forward(const Problem& pr, const void* Q, const void* K, cons
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (pr.d == 64)
-    e = pr.causal ? launch_fwd_t<64, true>(pr, mq, mk, mv, mo, L, stream)
-                  : launch_fwd_t<64, false>(pr, mq, mk, mv, mo, L, stream);
+    e = !pr.causal    ? launch_fwd_t<64, false, false>(pr, mq, mk, mv, mo, L, stream)
+        : pr.window ? launch_fwd_t<64, true, true>(pr, mq, mk, mv, mo, L, stream)
+                    : launch_fwd_t<64, true, false>(pr, mq, mk, mv, mo, L, stream);
   else
-    e = pr.causal ? launch_fwd_t<128, true>(pr, mq, mk, mv, mo, L, stream)
-                  : launch_fwd_t<128, false>(pr, mq, mk, mv, mo, L, stream);
+    e = !pr.causal    ? launch_fwd_t<128, false, false>(pr, mq, mk, mv, mo, L, stream)
+        : pr.window ? launch_fwd_t<128, true, true>(pr, mq, mk, mv, mo, L, stream)
+                    : launch_fwd_t<128, true, false>(pr, mq, mk, mv, mo, L, stream);
   if (e == cudaSuccess) ++*launches;
   return e;
 }
