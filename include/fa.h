@@ -34,9 +34,10 @@
  * A query row that sees no key gets O = 0, L = -inf, dQ = 0 and contributes
  * nothing to dK, dV.
  *
- * Supported: d == dv in {64, 128}.  Any B, Hq, Hkv, Tq, Tk >= 0 (ragged tails
+ * Supported: d and dv each in {64, 128} (dv may differ from d).  Any B, Hq, Hkv, Tq, Tk >= 0 (ragged tails
  * are handled; a zero-sized problem is a no-op; Tk == 0 yields O = 0 and
- * L = -inf).
+ * L = -inf), up to grid limits: Tq <= 65535 * 256, B * Hkv * ceil(Tk / 128)
+ * < 2^31, B * Hq < 2^31 (beyond them FA_ERR_UNSUPPORTED).
  *
  * Ownership and execution: the caller allocates and frees every buffer,
  * including the backward workspace.  The library never allocates or frees

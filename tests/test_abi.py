@@ -65,7 +65,9 @@ def test_invalid_dims_rejected(bad):
     assert call_fwd(dims(**bad)) == fa.FA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("bad", [dict(d=96, dv=96), dict(d=64, dv=128), dict(d=256, dv=256)])
+@pytest.mark.parametrize("bad", [dict(d=96, dv=96), dict(d=64, dv=96), dict(d=256, dv=256), dict(d=128, dv=32),
+                                 dict(Tq=65535 * 256 + 1),                       # forward grid limit
+                                 dict(B=1 << 12, Hq=1 << 12, Hkv=1 << 12, Tk=1 << 20)])  # backward grid limit
 def test_unsupported_dims(bad):
     assert call_fwd(dims(**bad)) == fa.FA_ERR_UNSUPPORTED
 

@@ -142,6 +142,35 @@ def test_rescale_on_some_rows_of_a_warp(fa, causal, window):
         assert_close(n, got[n], ref)
 
 
+MIXED = [
+    # B, Hq, Hkv, Tq, Tk, d, dv, causal, window
+    (1, 4, 2, 300, 333, 64, 128, False, 0),
+    (1, 4, 2, 300, 333, 128, 64, False, 0),
+    (2, 4, 1, 513, 513, 64, 128, True, 0),
+    (1, 2, 2, 200, 520, 128, 64, True, 0),     # causal Tq < Tk
+    (1, 2, 1, 600, 257, 64, 128, True, 0),     # causal Tq > Tk: empty first rows
+    (1, 4, 2, 700, 700, 128, 64, True, 200),   # with a sliding window
+]
+
+
+@pytest.mark.parametrize("shape", MIXED, ids=lambda s: "x".join(map(str, s[:5])) + f"_d{s[5]}dv{s[6]}" +
+                         ("c" if s[7] else "") + (f"w{s[8]}" if s[8] else ""))
+def test_value_head_size_differs_full_parity(fa, shape):
+    """V and O with a head size dv other than d (the page's forward reads the
+    value width from V's shape)."""
+    B, Hq, Hkv, Tq, Tk, d, dv, causal, W = shape
+    Q, K, V, dO = make_custom(B, Hq, Hkv, Tq, Tk, d, causal, seed=sum(shape[:7]), dv=dv)
+    assert V.shape[-1] == dv and dO.shape[-1] == dv
+    got = run_gpu(fa, Q, K, V, dO, causal, window=W)
+    O, L = oracle.forward(Q, K, V, causal, window=W)
+    dQ, dK, dV, _ = oracle.backward(Q, K, V, dO, causal, window=W)
+    assert got["O"].shape[-1] == dv and got["dV"].shape[-1] == dv and got["dK"].shape[-1] == d
+    assert_close("O", got["O"], O)
+    assert_L_close("L", got["L"], L)
+    for n, ref in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+        assert_close(n, got[n], ref)
+
+
 def test_window_requires_causal(fa):
     dev = torch.device("cuda")
     Q = torch.randn(1, 1, 64, 128, device=dev).to(torch.bfloat16)

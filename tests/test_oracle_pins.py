@@ -170,6 +170,15 @@ def pin_suite(lib, quick=False):
         for name, a, b in zip(("O", "L", "dQ", "dK", "dV"), (O, L, dQ, dK, dV), ref):
             if not np.all(np.isfinite(a)) or rel(a, b) > 1e-11:
                 failed.append(f"window:{name}:{n}")
+    # V and O narrower or wider than Q and K (d != dv), against torch float64
+    for n, (d, dv, causal) in enumerate(((8, 12, True), (12, 8, False))):
+        Q, K, V, dO = make(2, 4, 2, 19, 23, d, dv=dv, seed=300 + n)
+        O, L = lib.forward(Q, K, V, causal, 0.35)
+        dQ, dK, dV, _ = lib.backward(Q, K, V, dO, causal, 0.35)
+        ref = torch_reference(Q, K, V, dO, causal, 0.35)
+        for name, a, b in zip(("O", "L", "dQ", "dK", "dV"), (O, L, dQ, dK, dV), ref):
+            if a.shape != b.shape or not np.all(np.isfinite(a)) or rel(a, b) > 1e-11:
+                failed.append(f"dv:{name}:{n}")
     # finite differences on a tiny causal GQA problem
     Q, K, V, dO = make(1, 2, 1, 7, 7, 4, seed=99)
     for causal in (True, False):
@@ -343,6 +352,25 @@ def test_thread_count_does_not_change_results(oracle_lib):
         assert np.allclose(x, y, rtol=1e-14, atol=1e-15)
 
 
+@pytest.mark.parametrize("d,dv,causal", [(8, 16, True), (16, 8, True), (4, 12, False), (64, 128, True)])
+def test_value_head_size_differs(oracle_lib, d, dv, causal):
+    """V and O may have a head size dv other than d ("What Ordinary Autograd
+    Saves", section "The implementation under test": the value width is read
+    from V's shape): torch float64 and finite differences agree."""
+    Q, K, V, dO = make(1, 4, 2, 21, 26, d, dv=dv, seed=d * 100 + dv)
+    O, L = oracle_lib.forward(Q, K, V, causal, 0.3)
+    dQ, dK, dV, _ = oracle_lib.backward(Q, K, V, dO, causal, 0.3)
+    assert O.shape == (1, 4, 21, dv) and dQ.shape == Q.shape and dK.shape == K.shape and dV.shape == V.shape
+    Or, Lr, dQr, dKr, dVr = torch_reference(Q, K, V, dO, causal, 0.3)
+    assert rel(O, Or) < 1e-12 and rel(L, Lr) < 1e-12
+    assert rel(dQ, dQr) < 1e-11 and rel(dK, dKr) < 1e-11 and rel(dV, dVr) < 1e-11
+    if d <= 16:
+        Qs, Ks, Vs, dOs = (t[:, :2, :6] if t.shape[1] == 4 else t[:, :1, :6] for t in (Q, K, V, dO))
+        got = oracle_lib.backward(Qs, Ks, Vs, dOs, causal, 0.3)[:3]
+        for a, b in zip(got, fd_grads(oracle_lib, Qs, Ks, Vs, dOs, causal, 0.3)):
+            assert rel(a, b) < 1e-7
+
+
 @pytest.mark.parametrize("Tq,Tk,W", [(40, 40, 1), (40, 40, 7), (33, 70, 16), (70, 33, 5), (64, 64, 200)])
 def test_sliding_window_matches_torch_float64(oracle_lib, Tq, Tk, W):
     Q, K, V, dO = make(2, 4, 2, Tq, Tk, 8, seed=Tq + W)
@@ -452,6 +480,7 @@ MUTANTS = {
     "dP-wrong-operand": ("s += g[c] * v[c];", "s += g[c] * Kh[j * z.d + c];"),
     "dQ-uses-q": ("dq[c] += scale * dS * k[c];", "dq[c] += scale * dS * q[c];"),
     "window-off-by-one": ("- z.window + 1;", "- z.window;"),
+    "dP-over-d-not-dv": ("for (int c = 0; c < dv; ++c) s += g[c] * v[c];", "for (int c = 0; c < d; ++c) s += g[c] * v[c];"),
 }
 
 

@@ -47,16 +47,21 @@ fa_status check_dims(const fa_dims* dims, fa::Problem* pr) {
   if (z.window < 0 || (z.window > 0 && !z.causal)) return FA_ERR_INVALID_ARG;
   if (z.Hq > 0 && (z.Hkv < 1 || z.Hq % z.Hkv != 0)) return FA_ERR_INVALID_ARG;
   if (!(z.scale == z.scale) || std::isinf(z.scale)) return FA_ERR_INVALID_ARG;
-  if (z.dv != z.d || (z.d != 64 && z.d != 128)) return FA_ERR_UNSUPPORTED;
+  if ((z.d != 64 && z.d != 128) || (z.dv != 64 && z.dv != 128)) return FA_ERR_UNSUPPORTED;
   // TMA coordinates and grid dimensions are 32-bit; keep every index in range.
   if ((long long)z.B * z.Hq > 0x7fffffffLL || (long long)z.B * z.Hkv > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (z.Tq > (1 << 30) || z.Tk > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  // Grid limits: the forward's second grid dimension (pairs of 128-row query
+  // tiles) and the backward's linear grid of (batch, kv head, key tile) CTAs.
+  const long long q_pairs = ((long long)z.Tq + 255) / 256, kv_tiles = ((long long)z.Tk + 127) / 128;
+  if (q_pairs > 65535 || (long long)z.B * z.Hkv * kv_tiles > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   pr->B = z.B;
   pr->Hq = z.Hq;
   pr->Hkv = z.Hkv;
   pr->Tq = z.Tq;
   pr->Tk = z.Tk;
   pr->d = z.d;
+  pr->dv = z.dv;
   pr->causal = z.causal;
   // A window of Tk keys or more hides nothing (row i's window starts at or
   // before key i + Tk - Tq - Tk < 0); dropping it keeps kernel indices small.
@@ -121,9 +126,9 @@ fa_status fa_forward(const fa_dims* dims, const void* Q, const void* K, const vo
   fa::Problem pr;
   fa_status s = check_dims(dims, &pr);
   if (s != FA_OK) return s;
-  const long long nq = (long long)pr.B * pr.Hq * pr.Tq * pr.d;
-  const long long nk = (long long)pr.B * pr.Hkv * pr.Tk * pr.d;
-  if ((s = check_ptr(Q, nq)) || (s = check_ptr(K, nk)) || (s = check_ptr(V, nk)) || (s = check_ptr(O, nq)) ||
+  const long long nq = (long long)pr.B * pr.Hq * pr.Tq * pr.d, nqv = (long long)pr.B * pr.Hq * pr.Tq * pr.dv;
+  const long long nk = (long long)pr.B * pr.Hkv * pr.Tk * pr.d, nkv = (long long)pr.B * pr.Hkv * pr.Tk * pr.dv;
+  if ((s = check_ptr(Q, nq)) || (s = check_ptr(K, nk)) || (s = check_ptr(V, nkv)) || (s = check_ptr(O, nqv)) ||
       (s = check_ptr(L, (long long)pr.B * pr.Hq * pr.Tq)))
     return s;
   if (nq == 0) return FA_OK;
@@ -148,11 +153,11 @@ fa_status fa_backward_stages(const fa_dims* dims, const void* Q, const void* K, 
   fa_status s = check_dims(dims, &pr);
   if (s != FA_OK) return s;
   if (stages < 0 || stages > FA_BWD_ALL) return FA_ERR_INVALID_ARG;
-  const long long nq = (long long)pr.B * pr.Hq * pr.Tq * pr.d;
-  const long long nk = (long long)pr.B * pr.Hkv * pr.Tk * pr.d;
-  if ((s = check_ptr(Q, nq)) || (s = check_ptr(K, nk)) || (s = check_ptr(V, nk)) || (s = check_ptr(O, nq)) ||
-      (s = check_ptr(dO, nq)) || (s = check_ptr(L, (long long)pr.B * pr.Hq * pr.Tq)) || (s = check_ptr(dQ, nq)) ||
-      (s = check_ptr(dK, nk)) || (s = check_ptr(dV, nk)))
+  const long long nq = (long long)pr.B * pr.Hq * pr.Tq * pr.d, nqv = (long long)pr.B * pr.Hq * pr.Tq * pr.dv;
+  const long long nk = (long long)pr.B * pr.Hkv * pr.Tk * pr.d, nkv = (long long)pr.B * pr.Hkv * pr.Tk * pr.dv;
+  if ((s = check_ptr(Q, nq)) || (s = check_ptr(K, nk)) || (s = check_ptr(V, nkv)) || (s = check_ptr(O, nqv)) ||
+      (s = check_ptr(dO, nqv)) || (s = check_ptr(L, (long long)pr.B * pr.Hq * pr.Tq)) || (s = check_ptr(dQ, nq)) ||
+      (s = check_ptr(dK, nk)) || (s = check_ptr(dV, nkv)))
     return s;
   if ((nq == 0 && nk == 0) || stages == 0) return FA_OK;
   const size_t need = fa::backward_workspace_layout(pr).total;
@@ -182,7 +187,7 @@ const char* fa_status_string(fa_status s) {
       return "invalid argument (null or misaligned pointer, negative size, Hq not a multiple of Hkv, "
              "bad causal flag, window or scale, or workspace too small)";
     case FA_ERR_UNSUPPORTED:
-      return "unsupported shape (d must equal dv and be 64 or 128)";
+      return "unsupported shape (d and dv must each be 64 or 128; sizes within the grid limits)";
     case FA_ERR_CUDA:
       return "CUDA error while encoding tensor maps or launching kernels";
     case FA_ERR_TIMEOUT:

@@ -41,7 +41,7 @@
 //               own 128B-swizzled fp32 staging slots and adds each chunk into
 //               the fp32 accumulator in global memory with one TMA bulk
 //               reduce-add (32 x 32 box); no cross-warp synchronisation.
-// TMEM columns: S^T/P [0,128), dP^T/dQ [128,256), dV [256,256+d), dK [256+d, 256+2d).
+// TMEM columns: S^T/P [0,128), dP^T/dQ [128,256), dV [256,256+dv), dK [256+dv, 256+dv+d).
 #include <cstdint>
 
 #include "fa_internal.h"
@@ -55,16 +55,22 @@ constexpr int BM = fa::kTile;  // query rows per tile
 constexpr int BN = fa::kTile;  // keys per CTA
 constexpr int kThreads = 512;
 
-template <int HD>
+// HD: head size of Q and K; HDV: head size of V, O and dO.
+template <int HD, int HDV>
 struct BwdCfg {
-  static constexpr int TILE = 128 * HD * 2;  // one Q, dO, K or V tile (bf16)
+  static constexpr int QK_TILE = 128 * HD * 2;   // one Q or K tile (bf16)
+  static constexpr int VO_TILE = 128 * HDV * 2;  // one V or dO tile (bf16)
   static constexpr int DS_BYTES = BN * BM * 2;
   static constexpr int STG_SLOT = 32 * 32 * 4;  // one warp's 32 rows x 32 fp32 columns
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + TILE;
-  static constexpr int OFF_Q = OFF_V + TILE;       // [2]
-  static constexpr int OFF_DO = OFF_Q + 2 * TILE;  // [1]
-  static constexpr int OFF_DS = OFF_DO + TILE;
+  static constexpr int OFF_V = OFF_K + QK_TILE;
+  static constexpr int OFF_Q = OFF_V + VO_TILE;       // [2]
+  static constexpr int OFF_DO = OFF_Q + 2 * QK_TILE;  // [1]
+  static constexpr int OFF_DS = OFF_DO + VO_TILE;
+  // Epilogue staging of dV and dK over the Q ring and the dO buffer (idle by then).
+  static constexpr int OFF_DV_STAGE = OFF_Q;
+  static constexpr int OFF_DK_STAGE = OFF_Q + (QK_TILE > VO_TILE ? QK_TILE : VO_TILE);
+  static_assert(OFF_DK_STAGE + QK_TILE <= OFF_DS, "dV / dK staging fits in the Q ring and dO buffer");
   static constexpr int OFF_STG = OFF_DS + DS_BYTES;       // [4 warps][2] dQ staging slots
   static constexpr int OFF_LSE = OFF_STG + 8 * STG_SLOT;  // [2][128] fp32
   static constexpr int OFF_DELTA = OFF_LSE + 2 * 512;  // [2][128] fp32
@@ -74,11 +80,42 @@ struct BwdCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
+// Epilogue of one fp32 accumulator of W columns in TMEM (dV or dK): this
+// thread's key row r, the warpgroup's half of the columns (wg), times `mul`,
+// as bf16 into a 128-row, 128B-swizzled staging tile for the TMA store.
+// `have` is false when the CTA saw no query tile: the rows are zero.
+template <int W>
+__device__ __forceinline__ void stage_rows_bf16(uint32_t src, uint8_t* stage, int r, int wg, float mul, bool have) {
+  constexpr int HALF = W / 2;
+#pragma unroll
+  for (int c = 0; c < HALF / 32; ++c) {
+    uint32_t v[32];
+    if (have) {
+      tmem_ld32(src + c * 32, v);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = 0u;
+    }
+    const int col0 = wg * HALF + c * 32;  // first column of this chunk
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = pack_bf16x2(__uint_as_float(v[8 * q + 2 * e]) * mul, __uint_as_float(v[8 * q + 2 * e + 1]) * mul);
+      const int col = col0 + 8 * q;
+      st_shared_v4(smem_u32(stage + (col >> 6) * (BN * 128) + sw128_offset(r, (col & 63) >> 3)), w[0], w[1], w[2],
+                   w[3]);
+    }
+  }
+}
+
 struct BwdParams {
   const float* lse2;
   const float* delta;
   int* status;
-  int Hq, Hkv, G, Tq, Tk, causal_off, q_tiles;
+  int Hq, Hkv, G, Tq, Tk, causal_off, q_tiles, kv_tiles;
   int window;  // causal sliding window in keys, 0 = none
   long long Tq_pad;
   float scale_log2, scale;
@@ -86,13 +123,13 @@ struct BwdParams {
 
 // WINDOW (causal only): the sliding-window terms are compiled in only where
 // a window is set, so the plain causal and full masks keep their lean code.
-template <int HD, bool CAUSAL, bool WINDOW>
+template <int HD, int HDV, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                 const __grid_constant__ CUtensorMap tmAcc, const BwdParams p) {
-  using C = BwdCfg<HD>;
+  using C = BwdCfg<HD, HDV>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars + 0;
@@ -113,9 +150,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bkv = blockIdx.x;
+  // One linear grid, key tile slowest: every group's tile 0 runs first, then
+  // tile 1, ...  Causal low key tiles see the most query rows, so this is
+  // heaviest-first over the whole grid, which keeps the tail short.  (Ordering
+  // by group instead keeps each group's dQ accumulator in L2 and cuts DRAM
+  // traffic about 4x, but its late heavy CTAs make the causal step ~12% longer.)
+  const int n_groups = (int)(gridDim.x / p.kv_tiles);
+  const int n = blockIdx.x / n_groups;  // key tile
+  const int bkv = blockIdx.x - n * n_groups;
   const int b = bkv / p.Hkv, hk = bkv - b * p.Hkv;
-  const int n = blockIdx.y;  // key tile; causal: low tiles see the most query rows, run first
   const int k0 = n * BN;
 
   int m_begin = 0, m_end = p.q_tiles;
@@ -160,29 +203,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool run = (*abort_flag == 0) && T > 0;
-  const uint32_t T_S = tmem, T_DP = tmem + 128, T_DV = tmem + 256, T_DK = tmem + 256 + HD;
+  const uint32_t T_S = tmem, T_DP = tmem + 128, T_DV = tmem + 256, T_DK = tmem + 256 + HDV;
 
   if (warp < 4) {
     if (warp == 0 && lane == 0 && run) {
       // ---------------------------------------------------------- producer
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmdO);
-      mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+      mbar_arrive_expect_tx(kv_full, C::QK_TILE + C::VO_TILE);
 #pragma unroll
-      for (int cb = 0; cb < HD / 64; ++cb) {
-        tma_load_3d(smem + C::OFF_K + cb * BN * 128, &tmK, kv_full, cb * 64, k0, bkv);
-        tma_load_3d(smem + C::OFF_V + cb * BN * 128, &tmV, kv_full, cb * 64, k0, bkv);
-      }
+      for (int cb = 0; cb < HD / 64; ++cb) tma_load_3d(smem + C::OFF_K + cb * BN * 128, &tmK, kv_full, cb * 64, k0, bkv);
+#pragma unroll
+      for (int cb = 0; cb < HDV / 64; ++cb) tma_load_3d(smem + C::OFF_V + cb * BN * 128, &tmV, kv_full, cb * 64, k0, bkv);
       int last_q[2] = {-1, -1}, last_do = -1;
       for (int t = 0; t < T; ++t) {
         const int st = t & 1, u = t >> 1;
         const int g = t / n_m, m = m_begin + (t - g * n_m);
         const int bh = b * p.Hq + hk * p.G + g;
         if (!mbar_wait(&q_empty[st], (u & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&q_full[st], C::TILE + 1024);
+        mbar_arrive_expect_tx(&q_full[st], C::QK_TILE + 1024);
 #pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
-          tma_load_3d(smem + C::OFF_Q + st * C::TILE + cb * BM * 128, &tmQ, &q_full[st], cb * 64, m * BM, bh);
+          tma_load_3d(smem + C::OFF_Q + st * C::QK_TILE + cb * BM * 128, &tmQ, &q_full[st], cb * 64, m * BM, bh);
         const long long row0 = (long long)bh * p.Tq_pad + (long long)m * BM;
         bulk_load(smem + C::OFF_LSE + st * 512, p.lse2 + row0, 512, &q_full[st]);
         bulk_load(smem + C::OFF_DELTA + st * 512, p.delta + row0, 512, &q_full[st]);
@@ -190,11 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dO has one buffer, refilled only once dV_{t-1} is done: pull it into
         // L2 now so that its load later does not stall the dP MMA.
 #pragma unroll
-        for (int cb = 0; cb < HD / 64; ++cb) tma_prefetch_l2_3d(&tmdO, cb * 64, m * BM, bh);
+        for (int cb = 0; cb < HDV / 64; ++cb) tma_prefetch_l2_3d(&tmdO, cb * 64, m * BM, bh);
         if (!mbar_wait(do_empty, (t & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(do_full, C::TILE);
+        mbar_arrive_expect_tx(do_full, C::VO_TILE);
 #pragma unroll
-        for (int cb = 0; cb < HD / 64; ++cb)
+        for (int cb = 0; cb < HDV / 64; ++cb)
           tma_load_3d(smem + C::OFF_DO + cb * BM * 128, &tmdO, do_full, cb * 64, m * BM, bh);
         last_do = t;
       }
@@ -205,7 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1 && lane == 0 && run) {
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t id_sdp = idesc_bf16(BN, BM, 0, 0);  // S^T, dP^T: M = keys, N = queries
-      constexpr uint32_t id_kv = idesc_bf16(BN, HD, 0, 1);   // dV, dK: M = keys, N = d, B MN-major
+      constexpr uint32_t id_dv = idesc_bf16(BN, HDV, 0, 1);  // dV: M = keys, N = dv, B MN-major
+      constexpr uint32_t id_dk = idesc_bf16(BN, HD, 0, 1);   // dK: M = keys, N = d, B MN-major
       constexpr uint32_t id_q = idesc_bf16(BM, HD, 1, 1);    // dQ: M = queries (A MN-major), N = d
       const uint32_t k_base = smem_u32(smem + C::OFF_K), v_base = smem_u32(smem + C::OFF_V);
       const uint32_t ds_base = smem_u32(smem + C::OFF_DS);
@@ -213,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(kv_full, 0, abort_flag);
       for (int t = 0; ok && t < T; ++t) {
         const int st = t & 1, u = t >> 1;
-        const uint32_t q_base = smem_u32(smem + C::OFF_Q + st * C::TILE);
+        const uint32_t q_base = smem_u32(smem + C::OFF_Q + st * C::QK_TILE);
         if (!mbar_wait(&q_full[st], u & 1, abort_flag)) { ok = false; break; }
         if (t > 0 && !mbar_wait(tS_free, (t - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -226,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t > 0 && !mbar_wait(dq_empty, (t - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
+        for (int k = 0; k < HDV / 16; ++k)
           mma_ss(T_DP, desc_kmajor(v_base + (k >> 2) * (BN * 128) + (k & 3) * 32),
                  desc_kmajor(do_base + (k >> 2) * (BM * 128) + (k & 3) * 32), id_sdp, k > 0 ? 1u : 0u);
         mma_commit(dp_full);
@@ -237,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // overwrote its own half of S^T).
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
-          mma_ts(T_DV, T_S + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(do_base + k * 2048, BM * 128), id_kv,
+          mma_ts(T_DV, T_S + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(do_base + k * 2048, BM * 128), id_dv,
                  (t > 0 || k > 0) ? 1u : 0u);
         mma_commit(do_empty);
         if (!mbar_wait(ds_ready, t & 1, abort_flag)) { ok = false; break; }
@@ -246,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S^T columns: query columns [0,64) at [32,64), [64,128) at [96,128).
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
-          mma_ts(T_DK, T_S + (k >> 2) * 64 + 32 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_kv,
+          mma_ts(T_DK, T_S + (k >> 2) * 64 + 32 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_dk,
                  (t > 0 || k > 0) ? 1u : 0u);
         mma_commit(tS_free);  // P^T and dS^T (both in the S^T columns) consumed
         mma_commit(&q_empty[st]);
@@ -370,45 +413,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const bool mine = (T == 0 || ok) && *abort_flag == 0;
     if (named_bar_and(1, 256, mine)) {
-      constexpr int HALF = HD / 2;
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
-        uint8_t* stage = smem + C::OFF_Q + which * C::TILE;
-        const float mul = which ? p.scale : 1.f;
-        const uint32_t src = (which ? T_DK : T_DV) + lane_base + wg * HALF;
-#pragma unroll
-        for (int c = 0; c < HALF / 32; ++c) {
-          uint32_t v[32];
-          if (T > 0) {
-            tmem_ld32(src + c * 32, v);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = 0u;
-          }
-          const int col0 = wg * HALF + c * 32;  // first d column of this chunk
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(v[8 * q + 2 * e]) * mul, __uint_as_float(v[8 * q + 2 * e + 1]) * mul);
-            const int col = col0 + 8 * q;
-            st_shared_v4(smem_u32(stage + (col >> 6) * (BN * 128) + sw128_offset(r, (col & 63) >> 3)), w[0], w[1],
-                         w[2], w[3]);
-          }
-        }
-      }
+      stage_rows_bf16<HDV>(T_DV + lane_base + wg * (HDV / 2), smem + C::OFF_DV_STAGE, r, wg, 1.f, T > 0);
+      stage_rows_bf16<HD>(T_DK + lane_base + wg * (HD / 2), smem + C::OFF_DK_STAGE, r, wg, p.scale, T > 0);
       fence_async_smem();
       named_bar_sync(2, 256);
       if (warp == 4 && lane == 0) {
         prefetch_tmap(&tmdV);
         prefetch_tmap(&tmdK);
 #pragma unroll
-        for (int cb = 0; cb < HD / 64; ++cb) {
-          tma_store_3d(&tmdV, smem + C::OFF_Q + cb * BN * 128, cb * 64, k0, bkv);
-          tma_store_3d(&tmdK, smem + C::OFF_Q + C::TILE + cb * BN * 128, cb * 64, k0, bkv);
-        }
+        for (int cb = 0; cb < HDV / 64; ++cb)
+          tma_store_3d(&tmdV, smem + C::OFF_DV_STAGE + cb * BN * 128, cb * 64, k0, bkv);
+#pragma unroll
+        for (int cb = 0; cb < HD / 64; ++cb)
+          tma_store_3d(&tmdK, smem + C::OFF_DK_STAGE + cb * BN * 128, cb * 64, k0, bkv);
         bulk_commit();
         bulk_wait0();
       }
@@ -469,13 +486,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // D = rowsum(dO * O) and L2 = L * log2(e) per padded query row (padding rows:
-// D = 0, L2 = +inf); zeroes the row of the fp32 dQ accumulator.
-template <int HD>
+// D = 0, L2 = +inf); zeroes the row of the fp32 dQ accumulator.  HD: columns
+// of the accumulator (d); HDV: columns of O and dO (dv).
+template <int HD, int HDV>
 __global__ void __launch_bounds__(256) fa_bwd_pre(const uint16_t* __restrict__ O, const uint16_t* __restrict__ dO,
                                                   const float* __restrict__ L, float* __restrict__ lse2,
                                                   float* __restrict__ delta, float* __restrict__ dq_acc,
                                                   long long rows_pad, int Tq, long long Tq_pad) {
-  constexpr int PER = HD / 32;  // elements per lane
+  constexpr int PER = HDV / 32;  // O / dO elements per lane
+  constexpr int PERQ = HD / 32;  // accumulator elements per lane
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows_pad;
@@ -484,7 +503,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const uint16_t* __restrict__ O
     const long long q = row - bh * Tq_pad;
     float dot = 0.f;
     if (q < Tq) {
-      const long long src = (bh * Tq + q) * HD + lane * PER;
+      const long long src = (bh * Tq + q) * HDV + lane * PER;
       if (PER == 4) {
         const uint2 a = *reinterpret_cast<const uint2*>(O + src);
         const uint2 g = *reinterpret_cast<const uint2*>(dO + src);
@@ -507,8 +526,8 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const uint16_t* __restrict__ O
       delta[row] = dot;
       lse2[row] = q < Tq ? L[bh * Tq + q] * 1.4426950408889634f : __int_as_float(0x7f800000);
     }
-    float* acc = dq_acc + row * HD + lane * PER;
-    if (PER == 4)
+    float* acc = dq_acc + row * HD + lane * PERQ;
+    if (PERQ == 4)
       *reinterpret_cast<float4*>(acc) = make_float4(0.f, 0.f, 0.f, 0.f);
     else
       *reinterpret_cast<float2*>(acc) = make_float2(0.f, 0.f);
@@ -542,20 +561,28 @@ __global__ void fa_zero_words(uint32_t* p, size_t n) {
   for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n; t += (size_t)gridDim.x * blockDim.x) p[t] = 0u;
 }
 
-template <int HD, bool CAUSAL, bool WINDOW>
+template <int HD, int HDV, bool CAUSAL, bool WINDOW>
 cudaError_t launch_main_t(const fa::Problem& pr, const CUtensorMap* maps, const BwdParams& bp, cudaStream_t stream) {
-  using C = BwdCfg<HD>;
+  using C = BwdCfg<HD, HDV>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(fa_bwd_main<HD, CAUSAL, WINDOW>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaFuncSetAttribute(fa_bwd_main<HD, HDV, CAUSAL, WINDOW>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(pr.B * pr.Hkv, pr.kv_tiles());
-  fa_bwd_main<HD, CAUSAL, WINDOW><<<grid, kThreads, C::SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+  dim3 grid((unsigned)((long long)pr.B * pr.Hkv * pr.kv_tiles()));  // within int range (checked by the API)
+  fa_bwd_main<HD, HDV, CAUSAL, WINDOW><<<grid, kThreads, C::SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
                                                                maps[6], bp);
   return cudaGetLastError();
+}
+
+template <int HD, int HDV>
+cudaError_t launch_main_dims(const fa::Problem& pr, const CUtensorMap* maps, const BwdParams& bp,
+                             cudaStream_t stream) {
+  if (!pr.causal) return launch_main_t<HD, HDV, false, false>(pr, maps, bp, stream);
+  if (pr.window) return launch_main_t<HD, HDV, true, true>(pr, maps, bp, stream);
+  return launch_main_t<HD, HDV, true, false>(pr, maps, bp, stream);
 }
 
 inline int grid_for(long long work, int per_block) {
@@ -591,8 +618,8 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
     if (k_rows) {
       fa_zero_words<<<grid_for(k_rows * pr.d / 2, 256), 256, 0, stream>>>(static_cast<uint32_t*>(dK),
                                                                          (size_t)k_rows * pr.d / 2);
-      fa_zero_words<<<grid_for(k_rows * pr.d / 2, 256), 256, 0, stream>>>(static_cast<uint32_t*>(dV),
-                                                                         (size_t)k_rows * pr.d / 2);
+      fa_zero_words<<<grid_for(k_rows * pr.dv / 2, 256), 256, 0, stream>>>(static_cast<uint32_t*>(dV),
+                                                                          (size_t)k_rows * pr.dv / 2);
       *launches += 2;
     }
     if (q_rows) {
@@ -612,14 +639,10 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
   cudaError_t e = cudaSuccess;
   // 1. preprocess
   if (stages & FA_BWD_PRE) {
-  if (pr.d == 64)
-    fa_bwd_pre<64><<<grid_for(rows_pad, 8), 256, 0, stream>>>(static_cast<const uint16_t*>(O),
-                                                              static_cast<const uint16_t*>(dO), L, lse2, delta,
-                                                              dq_acc, rows_pad, pr.Tq, pr.Tq_pad());
-  else
-    fa_bwd_pre<128><<<grid_for(rows_pad, 8), 256, 0, stream>>>(static_cast<const uint16_t*>(O),
-                                                               static_cast<const uint16_t*>(dO), L, lse2, delta,
-                                                               dq_acc, rows_pad, pr.Tq, pr.Tq_pad());
+  auto pre = pr.d == 64 ? (pr.dv == 64 ? fa_bwd_pre<64, 64> : fa_bwd_pre<64, 128>)
+                        : (pr.dv == 64 ? fa_bwd_pre<128, 64> : fa_bwd_pre<128, 128>);
+  pre<<<grid_for(rows_pad, 8), 256, 0, stream>>>(static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), L,
+                                                 lse2, delta, dq_acc, rows_pad, pr.Tq, pr.Tq_pad());
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++*launches;
@@ -630,10 +653,10 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
   CUtensorMap maps[7];
   if (!encode_rows_bf16(&maps[0], Q, pr.d, pr.Tq, (long long)pr.B * pr.Hq) ||
       !encode_rows_bf16(&maps[1], K, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
-      !encode_rows_bf16(&maps[2], V, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
-      !encode_rows_bf16(&maps[3], dO, pr.d, pr.Tq, (long long)pr.B * pr.Hq) ||
+      !encode_rows_bf16(&maps[2], V, pr.dv, pr.Tk, (long long)pr.B * pr.Hkv) ||
+      !encode_rows_bf16(&maps[3], dO, pr.dv, pr.Tq, (long long)pr.B * pr.Hq) ||
       !encode_rows_bf16(&maps[4], dK, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
-      !encode_rows_bf16(&maps[5], dV, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
+      !encode_rows_bf16(&maps[5], dV, pr.dv, pr.Tk, (long long)pr.B * pr.Hkv) ||
       !encode_acc_f32(&maps[6], dq_acc, pr.d, pr.Tq_pad(), (long long)pr.B * pr.Hq, 32))
     return cudaErrorInvalidValue;
   BwdParams bp;
@@ -648,17 +671,15 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
   bp.causal_off = pr.Tk - pr.Tq;
   bp.window = pr.causal ? pr.window : 0;
   bp.q_tiles = pr.q_tiles();
+  bp.kv_tiles = pr.kv_tiles();
   bp.Tq_pad = pr.Tq_pad();
   bp.scale = pr.scale;
   bp.scale_log2 = pr.scale * 1.4426950408889634f;
   if (pr.d == 64)
-    e = !pr.causal    ? launch_main_t<64, false, false>(pr, maps, bp, stream)
-        : pr.window ? launch_main_t<64, true, true>(pr, maps, bp, stream)
-                    : launch_main_t<64, true, false>(pr, maps, bp, stream);
+    e = pr.dv == 64 ? launch_main_dims<64, 64>(pr, maps, bp, stream) : launch_main_dims<64, 128>(pr, maps, bp, stream);
   else
-    e = !pr.causal    ? launch_main_t<128, false, false>(pr, maps, bp, stream)
-        : pr.window ? launch_main_t<128, true, true>(pr, maps, bp, stream)
-                    : launch_main_t<128, true, false>(pr, maps, bp, stream);
+    e = pr.dv == 64 ? launch_main_dims<128, 64>(pr, maps, bp, stream)
+                    : launch_main_dims<128, 128>(pr, maps, bp, stream);
   if (e != cudaSuccess) return e;
   ++*launches;
   }

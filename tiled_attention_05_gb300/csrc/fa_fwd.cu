@@ -24,7 +24,7 @@
 //                rescale the O row in TMEM when the max grows by more than 2^8
 //                (lazy rescaling, exact after the final normalisation);
 //                epilogue O / l -> bf16 -> TMA store, L -> global.
-// TMEM columns: S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,256+d), O_B [384,384+d).
+// TMEM columns: S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,256+dv), O_B [384,384+dv).
 // Scores are kept in log2 units (scale * log2(e) folded into one FMA).
 //
 // Each tile visits the key tiles [beg, end) its rows can see (causal: up to
@@ -47,15 +47,21 @@ constexpr int BN = fa::kTile;  // keys per tile
 constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256 between rescales
 
-template <int HD>
+// HD: head size of Q and K (the score contraction); HDV: head size of V and O.
+template <int HD, int HDV>
 struct FwdCfg {
-  static constexpr int NS = HD == 64 ? 4 : 2;  // K/V ring depth
+  static constexpr int NS = (HD == 64 && HDV == 64) ? 4 : 2;  // K/V ring depth
   static constexpr int Q_BYTES = BM * HD * 2;
-  static constexpr int KV_BYTES = BN * HD * 2;
+  static constexpr int K_BYTES = BN * HD * 2;
+  static constexpr int V_BYTES = BN * HDV * 2;
+  static constexpr int O_BYTES = BM * HDV * 2;  // one tile's bf16 O, staged for its TMA store
+  static constexpr bool O_IN_Q = O_BYTES <= Q_BYTES;  // O staged in the tile's own (idle) Q buffer
   static constexpr int OFF_Q = 0;  // [2]: tile A, tile B
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
-  static constexpr int OFF_V = OFF_K + NS * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + NS * KV_BYTES;
+  static constexpr int OFF_V = OFF_K + NS * K_BYTES;
+  static constexpr int OFF_O = O_IN_Q ? OFF_Q : OFF_V + NS * V_BYTES;  // [2]
+  static constexpr int O_STRIDE = O_IN_Q ? Q_BYTES : O_BYTES;
+  static constexpr int OFF_BAR = O_IN_Q ? OFF_V + NS * V_BYTES : OFF_O + 2 * O_BYTES;
   static constexpr int NBAR = 1 + 4 * NS + 2 + 2 + 2 + 1;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -97,12 +103,12 @@ __device__ __forceinline__ void kv_range_for(const FwdParams& p, int qa, int* be
 
 // WINDOW (causal only): the sliding-window terms are compiled in only where
 // a window is set, so the plain causal and full masks keep their lean code.
-template <int HD, bool CAUSAL, bool WINDOW>
+template <int HD, int HDV, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const FwdParams p) {
-  using C = FwdCfg<HD>;
+  using C = FwdCfg<HD, HDV>;
   constexpr int NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -181,16 +187,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int jj = 0; jj < nkv_max; ++jj) {  // ring position jj holds key tile ub + jj
         const int s = jj % NS, u = jj / NS, kv0 = (ub + jj) * BN;
         if (!mbar_wait(&k_empty[s], (u & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&k_full[s], C::KV_BYTES);
+        mbar_arrive_expect_tx(&k_full[s], C::K_BYTES);
 #pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
-          tma_load_3d(smem + C::OFF_K + s * C::KV_BYTES + cb * BN * 128, &tmK, &k_full[s], cb * 64, kv0, bkv);
+          tma_load_3d(smem + C::OFF_K + s * C::K_BYTES + cb * BN * 128, &tmK, &k_full[s], cb * 64, kv0, bkv);
         k_last[s] = u;
         if (!mbar_wait(&v_empty[s], (u & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&v_full[s], C::KV_BYTES);
+        mbar_arrive_expect_tx(&v_full[s], C::V_BYTES);
 #pragma unroll
-        for (int cb = 0; cb < HD / 64; ++cb)
-          tma_load_3d(smem + C::OFF_V + s * C::KV_BYTES + cb * BN * 128, &tmV, &v_full[s], cb * 64, kv0, bkv);
+        for (int cb = 0; cb < HDV / 64; ++cb)
+          tma_load_3d(smem + C::OFF_V + s * C::V_BYTES + cb * BN * 128, &tmV, &v_full[s], cb * 64, kv0, bkv);
         v_last[s] = u;
       }
       // Every issued copy must land before the CTA releases its shared memory.
@@ -205,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && run) {
       constexpr uint32_t idS = idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t idPV = idesc_bf16(BM, HD, 0, 1);
+      constexpr uint32_t idPV = idesc_bf16(BM, HDV, 0, 1);
       const uint32_t k_base = smem_u32(smem + C::OFF_K);
       const uint32_t v_base = smem_u32(smem + C::OFF_V);
       bool ok = mbar_wait(q_full, 0, abort_flag);
@@ -220,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint64_t a = desc_kmajor(q_base + (k >> 2) * (BM * 128) + (k & 3) * 32);
-          const uint64_t bd = desc_kmajor(k_base + s * C::KV_BYTES + (k >> 2) * (BN * 128) + (k & 3) * 32);
+          const uint64_t bd = desc_kmajor(k_base + s * C::K_BYTES + (k >> 2) * (BN * 128) + (k & 3) * 32);
           mma_ss(tmem + x * 128, a, bd, idS, k > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[x]);
@@ -234,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t bd = desc_mnmajor(v_base + s * C::KV_BYTES + k * 2048, BN * 128);
+          const uint64_t bd = desc_mnmajor(v_base + s * C::V_BYTES + k * 2048, BN * 128);
           mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, bd, idPV, (j > kb[x] || k > 0) ? 1u : 0u);
         }
         return true;
@@ -344,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp_rescale) {
         const float a = rescale ? alpha : 1.f;
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = 0; c < HDV / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + c * 32, o);
           tmem_wait_ld();
@@ -369,9 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (named_bar_and(1 + x, 128, mine)) {
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       if (i < p.Tq) p.L[(size_t)bh * p.Tq + i] = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : NEG_INF;
-      uint8_t* Os = smem + C::OFF_Q + x * C::Q_BYTES;
+      uint8_t* Os = smem + C::OFF_O + x * C::O_STRIDE;
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < HDV / 32; ++c) {
         uint32_t o[32];
         if (nkv > 0) {
           tmem_ld32(tO + c * 32, o);
@@ -394,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (quad == 0 && lane == 0) {
         prefetch_tmap(&tmO);
 #pragma unroll
-        for (int cb = 0; cb < HD / 64; ++cb) tma_store_3d(&tmO, Os + cb * BM * 128, cb * 64, qx0, bh);
+        for (int cb = 0; cb < HDV / 64; ++cb) tma_store_3d(&tmO, Os + cb * BM * 128, cb * 64, qx0, bh);
         bulk_commit();
         bulk_wait0();
       }
@@ -409,13 +415,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_flag) atomicExch(p.status, DEV_TIMEOUT);
 }
 
-template <int HD, bool CAUSAL, bool WINDOW>
+template <int HD, int HDV, bool CAUSAL, bool WINDOW>
 cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mo, float* L, cudaStream_t stream) {
-  using C = FwdCfg<HD>;
+  using C = FwdCfg<HD, HDV>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<HD, CAUSAL, WINDOW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<HD, HDV, CAUSAL, WINDOW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -438,8 +444,16 @@ cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUt
   const char* wq = getenv("FA_TEST_WITHHOLD_Q");
   p.test_withhold_q = (wq && wq[0] == '1') ? 1 : 0;
   dim3 grid(pr.B * pr.Hq, (pr.q_tiles() + 1) / 2);
-  fa_fwd_kernel<HD, CAUSAL, WINDOW><<<grid, kThreads, C::SMEM, stream>>>(mq, mk, mv, mo, p);
+  fa_fwd_kernel<HD, HDV, CAUSAL, WINDOW><<<grid, kThreads, C::SMEM, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
+}
+
+template <int HD, int HDV>
+cudaError_t launch_fwd_dims(const fa::Problem& pr, const CUtensorMap& mq, const CUtensorMap& mk,
+                            const CUtensorMap& mv, const CUtensorMap& mo, float* L, cudaStream_t stream) {
+  if (!pr.causal) return launch_fwd_t<HD, HDV, false, false>(pr, mq, mk, mv, mo, L, stream);
+  if (pr.window) return launch_fwd_t<HD, HDV, true, true>(pr, mq, mk, mv, mo, L, stream);
+  return launch_fwd_t<HD, HDV, true, false>(pr, mq, mk, mv, mo, L, stream);
 }
 
 __global__ void fa_fwd_empty_keys(uint32_t* O_words, size_t n_words, float* L, size_t n_rows) {
@@ -460,7 +474,7 @@ cudaError_t launch_forward(const Problem& pr, const void* Q, const void* K, cons
   const long long rows = (long long)pr.B * pr.Hq * pr.Tq;
   if (rows == 0) return cudaSuccess;
   if (pr.Tk == 0) {
-    const size_t words = (size_t)rows * pr.d / 2;
+    const size_t words = (size_t)rows * pr.dv / 2;
     fa_fwd_empty_keys<<<1216, 256, 0, stream>>>(static_cast<uint32_t*>(O), words, L, (size_t)rows);
     ++*launches;
     return cudaGetLastError();
@@ -468,18 +482,16 @@ cudaError_t launch_forward(const Problem& pr, const void* Q, const void* K, cons
   CUtensorMap mq, mk, mv, mo;
   if (!encode_rows_bf16(&mq, Q, pr.d, pr.Tq, (long long)pr.B * pr.Hq) ||
       !encode_rows_bf16(&mk, K, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
-      !encode_rows_bf16(&mv, V, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
-      !encode_rows_bf16(&mo, O, pr.d, pr.Tq, (long long)pr.B * pr.Hq))
+      !encode_rows_bf16(&mv, V, pr.dv, pr.Tk, (long long)pr.B * pr.Hkv) ||
+      !encode_rows_bf16(&mo, O, pr.dv, pr.Tq, (long long)pr.B * pr.Hq))
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (pr.d == 64)
-    e = !pr.causal    ? launch_fwd_t<64, false, false>(pr, mq, mk, mv, mo, L, stream)
-        : pr.window ? launch_fwd_t<64, true, true>(pr, mq, mk, mv, mo, L, stream)
-                    : launch_fwd_t<64, true, false>(pr, mq, mk, mv, mo, L, stream);
+    e = pr.dv == 64 ? launch_fwd_dims<64, 64>(pr, mq, mk, mv, mo, L, stream)
+                    : launch_fwd_dims<64, 128>(pr, mq, mk, mv, mo, L, stream);
   else
-    e = !pr.causal    ? launch_fwd_t<128, false, false>(pr, mq, mk, mv, mo, L, stream)
-        : pr.window ? launch_fwd_t<128, true, true>(pr, mq, mk, mv, mo, L, stream)
-                    : launch_fwd_t<128, true, false>(pr, mq, mk, mv, mo, L, stream);
+    e = pr.dv == 64 ? launch_fwd_dims<128, 64>(pr, mq, mk, mv, mo, L, stream)
+                    : launch_fwd_dims<128, 128>(pr, mq, mk, mv, mo, L, stream);
   if (e == cudaSuccess) ++*launches;
   return e;
 }

@@ -10,7 +10,7 @@ namespace fa {
 constexpr int kTile = 128;  // rows of a query tile and of a key/value tile
 
 struct Problem {
-  int B, Hq, Hkv, Tq, Tk, d;
+  int B, Hq, Hkv, Tq, Tk, d, dv;  // d: Q/K head size, dv: V/O head size
   int causal;
   int window;   // causal sliding window in keys, 0 = none
   float scale;  // resolved (> 0)

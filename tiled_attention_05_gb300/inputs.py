@@ -29,10 +29,11 @@ class Workload:
     seed: int
     dO_std: float = 1.0
     window: int = 0  # causal sliding window in keys (0 = none)
+    dv_: int = 0     # head size of V and O when it differs from d (0 = same as d)
 
     @property
     def dv(self) -> int:
-        return self.d
+        return self.dv_ or self.d
 
     @property
     def G(self) -> int:
@@ -54,9 +55,12 @@ class Workload:
         return total
 
     def flops(self, part: str) -> float:
-        """Algorithmic flops: fwd 4*pairs*d, bwd 10*pairs*d, fwd+bwd 14*pairs*d per head."""
-        k = {"fwd": 4, "bwd": 10, "fwdbwd": 14}[part]
-        return float(k) * self.pairs_per_head() * self.d * self.B * self.Hq
+        """Algorithmic flops per head, two per multiply-add of each product:
+        fwd S = QK^T and O = PV: 2*pairs*(d + dv); bwd S, dP = dO V^T, dV, dK,
+        dQ: 2*pairs*(3 d + 2 dv).  With dv = d: 4, 10 and 14 * pairs * d."""
+        d, dv = self.d, self.dv
+        per_pair = {"fwd": 2 * (d + dv), "bwd": 2 * (3 * d + 2 * dv), "fwdbwd": 2 * (4 * d + 3 * dv)}[part]
+        return float(per_pair) * self.pairs_per_head() * self.B * self.Hq
 
     def as_dict(self) -> dict:
         return asdict(self)
@@ -94,7 +98,8 @@ def make_inputs(w: Workload, seed: int | None = None):
     return tuple(t.to(torch.bfloat16) for t in (Q, K, V, dO))
 
 
-def make_custom(B, Hq, Hkv, Tq, Tk, d, causal, seed, dO_std=1.0):
+def make_custom(B, Hq, Hkv, Tq, Tk, d, causal, seed, dO_std=1.0, dv=None):
     """Inputs for an ad-hoc shape (edge-case tests).  The draws do not depend
-    on the mask, so a windowed case takes the same inputs as its causal one."""
-    return make_inputs(Workload("custom", B, Hq, Hkv, Tq, Tk, d, causal, seed, dO_std))
+    on the mask, so a windowed case takes the same inputs as its causal one.
+    ``dv`` sets the head size of V and dO (default d)."""
+    return make_inputs(Workload("custom", B, Hq, Hkv, Tq, Tk, d, causal, seed, dO_std, dv_=dv or 0))
