@@ -228,9 +228,13 @@ def cpu_baseline_leg(w, cores, min_seconds=10.0):
     while n < groups and secs < min_seconds:
         f, dt, sw = time_oracle(w, None, cores, group=n)
         flops, secs, n = flops + f, secs + dt, n + 1
+    # context: the same oracle on one core, over a 2048-token prefix of one group
+    f1, dt1, sw1 = time_oracle(w, 2048, 1)
     return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} of {groups} GQA groups ({w.G} query heads each, all {w.Tq} rows, Tk={w.Tk}); "
-                      f"float64 forward + backward; {secs:.1f} s"}
+                      f"float64 forward + backward; {secs:.1f} s",
+            "one_core": {"value": f1 / dt1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                         "sample": f"one GQA group, Tq={sw1.Tq}, Tk={sw1.Tk}; {dt1:.1f} s"}}
 
 
 def host_cores():

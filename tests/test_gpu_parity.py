@@ -296,3 +296,25 @@ def test_workload_full_size(fa, name):
     # the whole output is finite
     for n in ("O", "L", "dQ", "dK", "dV"):
         assert torch.isfinite(got[n].float()).all(), n
+    check_full_tensor_invariants(w, got, V)
+
+
+def check_full_tensor_invariants(w, got, V):
+    """Properties of the exact result checked on every (batch, kv head) of the
+    full GPU tensors, not only on the sampled group:
+      * sum_j dS_ij = 0 for every row, so sum_j dK_j = 0 for every (b, kv head);
+        the GPU's deviation is the sum of its dK errors, bounded by Cauchy-Schwarz
+        through the rel-L2 bar: |sum_j dK_j| <= sqrt(Tk) * 1e-2 * ||dK||_F;
+      * every O row is a convex combination of V rows: each O column lies within
+        the range of that V column (up to bf16 rounding of O)."""
+    from tests.parity import REL_L2
+    dK = got["dK"].double()
+    col_sum = dK.sum(dim=2)                                  # [B, Hkv, d]
+    bound = math.sqrt(w.Tk) * REL_L2 * dK.pow(2).sum(dim=(2, 3)).sqrt()
+    assert bool((col_sum.norm(dim=-1) <= bound).all()), (col_sum.norm(dim=-1).max().item(), bound.min().item())
+    O = got["O"].double().view(w.B, w.Hkv, w.G, w.Tq, w.dv)
+    Vd = V.double()
+    vmin = Vd.amin(dim=2)[:, :, None, None, :]
+    vmax = Vd.amax(dim=2)[:, :, None, None, :]
+    slack = 2.0 ** -8 * torch.maximum(vmin.abs(), vmax.abs()) + 1e-6
+    assert bool(((O >= vmin - slack) & (O <= vmax + slack)).all())
