@@ -141,7 +141,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dp_full = bars + 8;
   uint64_t* p_ready = bars + 9;
   uint64_t* ds_ready = bars + 10;
-  uint64_t* tS_free = bars + 11;
   uint64_t* dq_full = bars + 12;
   uint64_t* dq_empty = bars + 13;
   uint64_t* acc_done = bars + 14;
@@ -187,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 256);
     mbar_init(ds_ready, 256);
-    mbar_init(tS_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(acc_done, 1);
@@ -253,18 +251,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t k_base = smem_u32(smem + C::OFF_K), v_base = smem_u32(smem + C::OFF_V);
       const uint32_t ds_base = smem_u32(smem + C::OFF_DS);
       const uint32_t do_base = smem_u32(smem + C::OFF_DO);
-      bool ok = mbar_wait(kv_full, 0, abort_flag);
-      for (int t = 0; ok && t < T; ++t) {
-        const int st = t & 1, u = t >> 1;
-        const uint32_t q_base = smem_u32(smem + C::OFF_Q + st * C::QK_TILE);
-        if (!mbar_wait(&q_full[st], u & 1, abort_flag)) { ok = false; break; }
-        if (t > 0 && !mbar_wait(tS_free, (t - 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+      // S^T(t) = K Q_t^T into T_S
+      auto mma_s = [&](int t) {
+        const uint32_t q_base = smem_u32(smem + C::OFF_Q + (t & 1) * C::QK_TILE);
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k)
           mma_ss(T_S, desc_kmajor(k_base + (k >> 2) * (BN * 128) + (k & 3) * 32),
                  desc_kmajor(q_base + (k >> 2) * (BM * 128) + (k & 3) * 32), id_sdp, k > 0 ? 1u : 0u);
         mma_commit(s_full);
+      };
+      // Issue order per tile t: dP^T, dV, dK, then S^T(t+1) and dQ(t).  At d = 64
+      // S^T(t+1) goes first: the MMA queue is shallow, so behind dQ it would wait
+      // for dQ to execute.  At d = 128 dQ goes first: running it beside the next
+      // tile's elementwise P phase (whose shared loads SS MMAs slow down) costs
+      // more than it saves (measured).  S^T(t+1) overwrites the P^T / dS^T
+      // columns that dK reads; one thread's MMAs execute in issue order, so dK
+      // has read them by then.
+      constexpr bool kNextSFirst = HD == 64;
+      bool ok = mbar_wait(kv_full, 0, abort_flag) && mbar_wait(&q_full[0], 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        mma_s(0);
+      }
+      for (int t = 0; ok && t < T; ++t) {
+        const int st = t & 1;
+        const uint32_t q_base = smem_u32(smem + C::OFF_Q + st * C::QK_TILE);
+        // dP^T shares its TMEM columns with dQ: the previous tile's dQ must be drained
         if (!mbar_wait(do_full, t & 1, abort_flag)) { ok = false; break; }
         if (t > 0 && !mbar_wait(dq_empty, (t - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -291,13 +303,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < BM / 16; ++k)
           mma_ts(T_DK, T_S + (k >> 2) * 64 + 32 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_dk,
                  (t > 0 || k > 0) ? 1u : 0u);
-        mma_commit(tS_free);  // P^T and dS^T (both in the S^T columns) consumed
         mma_commit(&q_empty[st]);
+        auto next_s = [&]() -> bool {
+          if (t + 1 >= T) return true;
+          if (!mbar_wait(&q_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort_flag)) return false;
+          tc_fence_after();
+          mma_s(t + 1);
+          return true;
+        };
+        if (kNextSFirst && !next_s()) { ok = false; break; }
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
           mma_ss(T_DP, desc_mnmajor(ds_base + k * 2048, BN * 128), desc_mnmajor(k_base + k * 2048, BN * 128), id_q,
                  k > 0 ? 1u : 0u);
         mma_commit(dq_full);
+        if (!kNextSFirst && !next_s()) { ok = false; break; }
       }
       mma_commit(acc_done);
       mma_commit(drain);
