@@ -391,8 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(p_ready);
       // ---- dS = P * (dP - D) -> shared memory (row = key, 128B-swizzled, query-contiguous)
-      // dP^T is in TMEM, and the dK / dQ MMAs of the previous tile are done reading dS
-      got = mbar_wait(dp_full, t & 1, abort_flag) && (t == 0 || mbar_wait(dq_full, (t - 1) & 1, abort_flag));
+      // dP^T is in TMEM.  The previous tile's dQ MMA, which reads dS from shared
+      // memory, was issued before this tile's dP^T by the same thread, so the
+      // dP^T commit covers it too.
+      got = mbar_wait(dp_full, t & 1, abort_flag);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after();
       uint8_t* ds_blk = smem + C::OFF_DS + wg * (BN * 128);
