@@ -218,9 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) tc_fence_after();
       auto active = [&](int x, int j) { return j >= kb[x] && j < ke[x]; };
       // S_X(j) = Q_X K_j^T into TMEM [128 X, 128 X + 128)
+      // Tile B's groups use the K_j / V_j tile A's groups have just waited
+      // for; re-waiting would only leave the tensor pipe idle for the round trip.
       auto issue_s = [&](int x, int j) -> bool {
         const int s = (j - ub) % NS;
-        if (!mbar_wait(&k_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
+        if (!(x == 1 && active(0, j)) && !mbar_wait(&k_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t q_base = smem_u32(smem + C::OFF_Q + x * C::Q_BYTES);
 #pragma unroll
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int x, int j) -> bool {
         const int s = (j - ub) % NS;
         if (!mbar_wait(&p_full[x], (j - kb[x]) & 1, abort_flag)) return false;
-        if (!mbar_wait(&v_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
+        if (!(x == 1 && active(0, j)) && !mbar_wait(&v_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
