@@ -156,6 +156,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain, 1);
     fence_mbar_init();
+    // The first loads (Q_A, Q_B and the first NS key/value tiles, whose ring
+    // slots are free) are issued here, before TMEM allocation and the CTA-wide
+    // barrier, so their memory latency overlaps the set-up.
+    if (*abort_flag == 0 && nkv_max > 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      if (!p.test_withhold_q) {
+        mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_BYTES);
+#pragma unroll
+        for (int cb = 0; cb < HD / 64; ++cb) {
+          tma_load_3d(smem + C::OFF_Q + cb * BM * 128, &tmQ, q_full, cb * 64, q0, bh);
+          if (has_b) tma_load_3d(smem + C::OFF_Q + C::Q_BYTES + cb * BM * 128, &tmQ, q_full, cb * 64, q0 + BM, bh);
+        }
+      }
+      for (int jj = 0; jj < NS && jj < nkv_max; ++jj) {
+        const int kv0 = (ub + jj) * BN;
+        mbar_arrive_expect_tx(&k_full[jj], C::K_BYTES);
+#pragma unroll
+        for (int cb = 0; cb < HD / 64; ++cb)
+          tma_load_3d(smem + C::OFF_K + jj * C::K_BYTES + cb * BN * 128, &tmK, &k_full[jj], cb * 64, kv0, bkv);
+        mbar_arrive_expect_tx(&v_full[jj], C::V_BYTES);
+#pragma unroll
+        for (int cb = 0; cb < HDV / 64; ++cb)
+          tma_load_3d(smem + C::OFF_V + jj * C::V_BYTES + cb * BN * 128, &tmV, &v_full[jj], cb * 64, kv0, bkv);
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -170,21 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && run) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      if (!p.test_withhold_q) {
-        mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_BYTES);
-#pragma unroll
-        for (int cb = 0; cb < HD / 64; ++cb) {
-          tma_load_3d(smem + C::OFF_Q + cb * BM * 128, &tmQ, q_full, cb * 64, q0, bh);
-          if (has_b) tma_load_3d(smem + C::OFF_Q + C::Q_BYTES + cb * BM * 128, &tmQ, q_full, cb * 64, q0 + BM, bh);
-        }
-      }
+      // Q and the first NS key/value tiles were issued during set-up.
       int k_last[NS], v_last[NS];
 #pragma unroll
-      for (int s = 0; s < NS; ++s) k_last[s] = v_last[s] = -1;
-      for (int jj = 0; jj < nkv_max; ++jj) {  // ring position jj holds key tile ub + jj
+      for (int s = 0; s < NS; ++s) k_last[s] = v_last[s] = s < nkv_max ? 0 : -1;
+      for (int jj = NS; jj < nkv_max; ++jj) {  // ring position jj holds key tile ub + jj
         const int s = jj % NS, u = jj / NS, kv0 = (ub + jj) * BN;
         if (!mbar_wait(&k_empty[s], (u & 1) ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(&k_full[s], C::K_BYTES);
