@@ -202,6 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const bool run = (*abort_flag == 0) && T > 0;
   const uint32_t T_S = tmem, T_DP = tmem + 128, T_DV = tmem + 256, T_DK = tmem + 256 + HDV;
+  // dQ shares dP^T's columns unless there is room for columns of its own
+  // (d = 64: dK ends at 384 or 448); then dP^T(t+1) need not wait for dQ(t)'s
+  // drain, only dQ(t+1) does.
+  constexpr bool kOwnDQ = 256 + HDV + 2 * HD <= 512;
+  const uint32_t T_DQ = kOwnDQ ? T_DK + HD : T_DP;
 
   if (warp < 4) {
     if (warp == 0 && lane == 0 && run) {
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q_base = smem_u32(smem + C::OFF_Q + st * C::QK_TILE);
         // dP^T shares its TMEM columns with dQ: the previous tile's dQ must be drained
         if (!mbar_wait(do_full, t & 1, abort_flag)) { ok = false; break; }
-        if (t > 0 && !mbar_wait(dq_empty, (t - 1) & 1, abort_flag)) { ok = false; break; }
+        if (!kOwnDQ && t > 0 && !mbar_wait(dq_empty, (t - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < HDV / 16; ++k)
@@ -312,9 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         };
         if (kNextSFirst && !next_s()) { ok = false; break; }
+        if (kOwnDQ && t > 0) {  // dQ(t-1) drained from its columns
+          if (!mbar_wait(dq_empty, (t - 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+        }
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          mma_ss(T_DP, desc_mnmajor(ds_base + k * 2048, BN * 128), desc_mnmajor(k_base + k * 2048, BN * 128), id_q,
+          mma_ss(T_DQ, desc_mnmajor(ds_base + k * 2048, BN * 128), desc_mnmajor(k_base + k * 2048, BN * 128), id_q,
                  k > 0 ? 1u : 0u);
         mma_commit(dq_full);
         if (!kNextSFirst && !next_s()) { ok = false; break; }
@@ -471,12 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < NCH; c += 2) {
         uint32_t v0[32], v1[32];
-        tmem_ld32(T_DP + lane_base + c * 32, v0);
-        tmem_ld32(T_DP + lane_base + (c + 1) * 32, v1);
+        tmem_ld32(T_DQ + lane_base + c * 32, v0);
+        tmem_ld32(T_DQ + lane_base + (c + 1) * 32, v1);
         tmem_wait_ld();
         if (c + 2 >= NCH) {
           tc_fence_before();
-          mbar_arrive(dq_empty);  // all of dQ_t is out of TMEM: it may take dP_{t+1}
+          mbar_arrive(dq_empty);  // all of dQ_t is out of TMEM: it may take dP_{t+1} (or dQ_{t+1})
         }
         if (leader) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // both slots read
         __syncwarp();
