@@ -34,8 +34,8 @@ METRIC = "attention fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor 
 # workload, from one ncu capture (profiles/fa_bwd_main_<workload>.md).  Valid
 # only for the source it was taken on: reported as null once that changes.
 NCU_TRAFFIC = {
-    "gqa_B2_H32x8_T8192_d128_causal": {"bytes": 2367876000 + 1171273000, "source_sha256_16": "b0798ab8c6f864b3"},
-    "swa_B1_H32x8_T8192_W2080_d128": {"bytes": 445266432 + 189772544, "source_sha256_16": "b0798ab8c6f864b3"},
+    "gqa_B2_H32x8_T8192_d128_causal": {"bytes": 2373067000 + 1158211000, "source_sha256_16": "ac54cec906707ea8"},
+    "swa_B1_H32x8_T8192_W2080_d128": {"bytes": 446134784 + 191012608, "source_sha256_16": "ac54cec906707ea8"},
 }
 TRAFFIC_SOURCES = ("tiled_attention_05_gb300/csrc/fa_bwd.cu", "tiled_attention_05_gb300/csrc/sm103_ptx.cuh")
 

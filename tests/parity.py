@@ -47,7 +47,9 @@ def errors(gpu, ref) -> dict:
         "max_ref": float(np.abs(r[fin]).max()) if fin.any() else 0.0,
         # the error in units of the reference's bf16 ulp, and how many references are >= 8 in magnitude
         # (where half a bf16 ulp alone is 1/64 or more), so a miss of the bare bar shows as rounding-limited
-        "max_err_bf16_ulps": float((d / np.maximum(2.0 * half_ulp_bf16(r[fin]), 2.0 ** -133)).max()) if d.size else 0.0,
+        # (ulps taken at max(|ref|, 1e-3 * max|ref|), so exact zeros in the reference do not divide by zero)
+        "max_err_bf16_ulps": float((d / (2.0 * half_ulp_bf16(np.maximum(np.abs(r[fin]), 1e-3 * np.abs(r[fin]).max())))).max())
+        if d.size and np.abs(r[fin]).max() > 0 else 0.0,
         "n_ref_ge_8": int(np.sum(np.abs(r[fin]) >= 8.0)),
     }
 
