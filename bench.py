@@ -30,27 +30,37 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
 
-# DRAM bytes (read + write) of one launch of the dominant kernel on the headline
-# workload, from one ncu capture (profiles/fa_bwd_main_<workload>.md).  Valid
-# only for the source it was taken on: reported as null once that changes.
+# DRAM bytes (read + write) of one launch of the dominant kernel, from one ncu
+# capture per workload (profiles/fa_bwd_main_<workload>.md).  Valid only for the
+# kernel code it was taken on (comments aside): reported as null once that changes.
 NCU_TRAFFIC = {
-    "gqa_B2_H32x8_T8192_d128_causal": {"bytes": 2373067000 + 1158211000, "source_sha256_16": "ac54cec906707ea8"},
-    "swa_B1_H32x8_T8192_W2080_d128": {"bytes": 446134784 + 191012608, "source_sha256_16": "ac54cec906707ea8"},
+    "gqa_B2_H32x8_T8192_d128_causal": {"bytes": 2373067000 + 1158211000, "source_sha256_16": "cd67545a182d2c4a"},
+    "swa_B1_H32x8_T8192_W2080_d128": {"bytes": 446134784 + 191012608, "source_sha256_16": "cd67545a182d2c4a"},
 }
 TRAFFIC_SOURCES = ("tiled_attention_05_gb300/csrc/fa_bwd.cu", "tiled_attention_05_gb300/csrc/sm103_ptx.cuh")
 
 
-def measured_traffic(workload: str):
+def source_code_hash(paths=TRAFFIC_SOURCES) -> str:
+    """sha256[:16] of the kernel sources with comments and whitespace removed,
+    so that a comment-only edit does not detach a recorded measurement."""
     import hashlib
+    import re
 
+    h = hashlib.sha256()
+    for f in paths:
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(re.sub(r"\s+", "", text).encode())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
     rec = NCU_TRAFFIC.get(workload)
     if rec is None:
         return None
-    h = hashlib.sha256()
-    for f in TRAFFIC_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
-    return rec["bytes"] if h.hexdigest()[:16] == rec["source_sha256_16"] else None
+    return rec["bytes"] if source_code_hash() == rec["source_sha256_16"] else None
 
 
 FLUSH_BYTES = 256 << 20

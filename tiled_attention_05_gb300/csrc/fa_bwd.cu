@@ -29,8 +29,11 @@
 //                 dP^T = V dO_t^T       -> TMEM [128,256)
 //                 dV  += P^T dO_t       A = P^T from TMEM (bf16, written over S^T)
 //                 dK  += dS^T Q_t       A = dS^T from TMEM (bf16, the other half of S^T)
-//                 dQ_t = dS K           -> TMEM [128,128+d)  A = the same dS bytes
+//                 dQ_t = dS K           -> TMEM [128,128+d), or at d = 64 the free
+//                                        columns after dK; A = the same dS bytes
 //                                        read MN-major; B = K read MN-major
+//               with S^T(t+1) issued right after dK(t) (d = 64) or dQ(t) (d = 128),
+//               relying on in-order MMA execution rather than a wait.
 //   warps 4..11 two elementwise warpgroups (thread = key row = TMEM lane; group
 //               w owns query columns [64w, 64w+64)): P = exp2(S*scale*log2e - L2)
 //               with masks -> TMEM; dS = P * (dP - D) -> shared memory (for the
@@ -41,7 +44,8 @@
 //               own 128B-swizzled fp32 staging slots and adds each chunk into
 //               the fp32 accumulator in global memory with one TMA bulk
 //               reduce-add (32 x 32 box); no cross-warp synchronisation.
-// TMEM columns: S^T/P [0,128), dP^T/dQ [128,256), dV [256,256+dv), dK [256+dv, 256+dv+d).
+// TMEM columns: S^T/P [0,128), dP^T/dQ [128,256), dV [256,256+dv), dK [256+dv, 256+dv+d);
+// at d = 64 dQ moves to [256+dv+d, 256+dv+2d).
 #include <cstdint>
 
 #include "fa_internal.h"
