@@ -254,8 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O_X += P_X(j) V_j with P_X read from TMEM (packed bf16 over S_X)
       auto issue_pv = [&](int x, int j) -> bool {
         const int s = (j - ub) % NS;
-        if (!mbar_wait(&p_full[x], (j - kb[x]) & 1, abort_flag)) return false;
+        // V_j has almost always landed: check it first, so that once P_X(j) is
+        // ready the MMAs go out without another round trip.
         if (!(x == 1 && active(0, j)) && !mbar_wait(&v_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
+        if (!mbar_wait(&p_full[x], (j - kb[x]) & 1, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
