@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dp_full = bars + 8;
   uint64_t* p_ready = bars + 9;
   uint64_t* ds_ready = bars + 10;
+  uint64_t* ds_half = bars + 11;  // dS^T of each warpgroup's first 32 query columns is in TMEM
   uint64_t* dq_full = bars + 12;
   uint64_t* dq_empty = bars + 13;
   uint64_t* acc_done = bars + 14;
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 256);
     mbar_init(ds_ready, 256);
+    mbar_init(ds_half, 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(acc_done, 1);
@@ -304,14 +306,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(T_DV, T_S + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(do_base + k * 2048, BM * 128), id_dv,
                  (t > 0 || k > 0) ? 1u : 0u);
         mma_commit(do_empty);
-        if (!mbar_wait(ds_ready, t & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
         // dS^T lives in TMEM too, packed into the other half of each group's
         // S^T columns: query columns [0,64) at [32,64), [64,128) at [96,128).
+        // K steps 0, 1, 4, 5 (each warpgroup's first 32 query columns) go as
+        // soon as that half is written; 2, 3, 6, 7 once all of dS is.
+        if (!mbar_wait(ds_half, t & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
-          mma_ts(T_DK, T_S + (k >> 2) * 64 + 32 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_dk,
-                 (t > 0 || k > 0) ? 1u : 0u);
+          if ((k & 3) < 2)
+            mma_ts(T_DK, T_S + (k >> 2) * 64 + 32 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_dk,
+                   (t > 0 || k > 0) ? 1u : 0u);
+        if (!mbar_wait(ds_ready, t & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BM / 16; ++k)
+          if ((k & 3) >= 2)
+            mma_ts(T_DK, T_S + (k >> 2) * 64 + 32 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_dk, 1u);
         mma_commit(&q_empty[st]);
         auto next_s = [&]() -> bool {
           if (t + 1 >= T) return true;
@@ -434,6 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           st_shared_v4(smem_u32(ds_blk + sw128_offset(r, ch * 4 + cc)), w[0], w[1], w[2], w[3]);
           // packed dS^T of these 8 columns, for the dK MMA (A from TMEM)
           tmem_st4(T_S + lane_base + wg * 64 + 32 + ch * 16 + cc * 4, w[0], w[1], w[2], w[3]);
+        }
+        if (ch == 0) {  // first half of dS^T in TMEM: the dK MMA may start on it
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(ds_half);
         }
       }
       tmem_wait_st();
