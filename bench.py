@@ -34,8 +34,8 @@ METRIC = "attention fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor 
 # capture per workload (profiles/fa_bwd_main_<workload>.md).  Valid only for the
 # kernel code it was taken on (comments aside): reported as null once that changes.
 NCU_TRAFFIC = {
-    "gqa_B2_H32x8_T8192_d128_causal": {"bytes": 2373067000 + 1158211000, "source_sha256_16": "cd67545a182d2c4a"},
-    "swa_B1_H32x8_T8192_W2080_d128": {"bytes": 446134784 + 191012608, "source_sha256_16": "cd67545a182d2c4a"},
+    "gqa_B2_H32x8_T8192_d128_causal": {"bytes": 2430414000 + 1189226000, "source_sha256_16": "768ef41be5b49726"},
+    "swa_B1_H32x8_T8192_W2080_d128": {"bytes": 446253568 + 190739712, "source_sha256_16": "768ef41be5b49726"},
 }
 TRAFFIC_SOURCES = ("tiled_attention_05_gb300/csrc/fa_bwd.cu", "tiled_attention_05_gb300/csrc/sm103_ptx.cuh")
 
