@@ -31,8 +31,8 @@ if ROOT not in sys.path:
 METRIC = "attention fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from one ncu
-# capture per workload (profiles/fa_bwd_main_<workload>.md).  Valid only for the
-# kernel code it was taken on (comments aside): reported as null once that changes.
+# capture of it on each workload listed.  Valid only for the kernel code it was
+# taken on (comments aside): reported as null once that changes.
 NCU_TRAFFIC = {
     "gqa_B2_H32x8_T8192_d128_causal": {"bytes": 2430414000 + 1189226000, "source_sha256_16": "768ef41be5b49726"},
     "swa_B1_H32x8_T8192_W2080_d128": {"bytes": 446253568 + 190739712, "source_sha256_16": "768ef41be5b49726"},

@@ -22,7 +22,7 @@ struct Problem {
 
 // Encodes a TMA descriptor for a contiguous bf16 tensor viewed as
 // [outer][rows][inner] (inner contiguous), box = 64 x 128 x 1, 128-byte swizzle.
-// Returns false if the driver rejects it.
+// Returns false if cuTensorMapEncodeTiled rejects it.
 bool encode_rows_bf16(CUtensorMap* map, const void* base, int inner, int rows, long long outer);
 
 // TMA descriptor for the fp32 dQ accumulator viewed as [outer][rows][inner]
