@@ -318,3 +318,40 @@ def check_full_tensor_invariants(w, got, V):
     vmax = Vd.amax(dim=2)[:, :, None, None, :]
     slack = 2.0 ** -8 * torch.maximum(vmin.abs(), vmax.abs()) + 1e-6
     assert bool(((O >= vmin - slack) & (O <= vmax + slack)).all())
+
+
+POISON = [
+    # B, Hq, Hkv, Tq, Tk, d, dv, causal, window
+    (1, 2, 1, 300, 333, 128, 128, False, 0),   # ragged tails on both sides
+    (1, 2, 2, 513, 257, 64, 64, True, 0),      # empty first rows (Tq > Tk, causal)
+    (2, 4, 2, 200, 520, 128, 64, True, 0),     # Tq < Tk, dv != d
+    (1, 4, 1, 700, 700, 64, 128, True, 200),   # sliding window, dv != d, GQA 4:1
+]
+
+
+@pytest.mark.parametrize("shape", POISON, ids=lambda s: "x".join(map(str, s[:7])) + ("c" if s[7] else "") +
+                         (f"w{s[8]}" if s[8] else ""))
+def test_every_output_element_is_written(fa, shape):
+    """Output buffers filled with NaN before the call: any element a kernel
+    does not write (a missed tile, a padding row, a skipped window tile) stays
+    NaN and fails; the written values must also match the oracle."""
+    B, Hq, Hkv, Tq, Tk, d, dv, causal, W = shape
+    Q, K, V, dO = make_custom(B, Hq, Hkv, Tq, Tk, d, causal, seed=sum(shape[:7]) + 17, dv=dv)
+    dev = torch.device("cuda")
+    Qd, Kd, Vd, dOd = (t.to(dev) for t in (Q, K, V, dO))
+    nan = float("nan")
+    O = torch.full((B, Hq, Tq, dv), nan, dtype=torch.bfloat16, device=dev)
+    L = torch.full((B, Hq, Tq), nan, dtype=torch.float32, device=dev)
+    dQ, dK, dV = (torch.full_like(t, nan) for t in (Qd, Kd, Vd))
+    fa.fa_forward(Qd, Kd, Vd, causal, O=O, L=L, window=W)
+    fa.fa_backward(Qd, Kd, Vd, O, dOd, L, causal, dQ=dQ, dK=dK, dV=dV, window=W)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == 0
+    for n, t in (("O", O), ("L", L), ("dQ", dQ), ("dK", dK), ("dV", dV)):
+        assert not torch.isnan(t.float()).any(), f"{n} has unwritten (NaN) elements"
+    Or, Lr = oracle.forward(Q, K, V, causal, window=W)
+    dQr, dKr, dVr, _ = oracle.backward(Q, K, V, dO, causal, window=W)
+    assert_close("O", O.cpu(), Or)
+    assert_L_close("L", L.cpu(), Lr)
+    for n, g, r in (("dQ", dQ, dQr), ("dK", dK, dKr), ("dV", dV, dVr)):
+        assert_close(n, g.cpu(), r)
