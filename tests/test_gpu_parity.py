@@ -98,6 +98,9 @@ WINDOWED = [
     (2, 4, 1, 1000, 1000, 128, 333),   # GQA 4:1, window start off the tile grid
     (1, 4, 4, 384, 384, 64, 129),      # tile multiples, window one past a tile
     (1, 2, 1, 300, 300, 128, 5000),    # window longer than Tk: plain causal
+    (1, 8, 2, 1, 5000, 128, 300),      # one appended query over a long prefix, windowed
+    (1, 2, 1, 3, 2000, 64, 1),         # three queries, each sees only its own position
+    (2, 4, 2, 40, 90, 128, 70),        # window reaching past the start of a short prefix
 ]
 
 
