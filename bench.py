@@ -304,7 +304,7 @@ def run_ours(args, w):
 
     Qh, Kh, Vh, dOh = make_inputs(w)
     Q, K, V, dO = (t.to(dev) for t in (Qh, Kh, Vh, dOh))
-    O = torch.empty_like(Q)
+    O = torch.empty_like(dO)  # [B, Hq, Tq, dv]
     L = torch.empty(w.B, w.Hq, w.Tq, dtype=torch.float32, device=dev)
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     dims = fa.make_dims(w.B, w.Hq, w.Hkv, w.Tq, w.Tk, w.d, w.dv, w.causal, None, w.window)

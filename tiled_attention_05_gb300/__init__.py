@@ -111,8 +111,24 @@ def _check(t: torch.Tensor, name: str, dtype=torch.bfloat16):
         raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
 
 
-def _stream_ptr(stream=None) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream()
+def _check_all(device, specs):
+    """The library sees only pointers, so every size it relies on is checked
+    here: each (tensor, name, shape, dtype) must have exactly that shape, be a
+    contiguous CUDA tensor of that dtype and live on ``device``.  Shapes are
+    checked first so a mismatch is reported as such on any device."""
+    for t, name, shape, _ in specs:
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    for t, name, _, dtype in specs:
+        _check(t, name, dtype)
+        if t.device != device:
+            raise ValueError(f"{name} is on {t.device}, expected {device} (all tensors on one GPU)")
+
+
+def _stream_ptr(stream=None, device=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    if device is not None and s.device != device:
+        raise ValueError(f"stream belongs to {s.device}, the tensors to {device}")
     return s.cuda_stream
 
 
@@ -128,18 +144,22 @@ def fa_backward_workspace_bytes(dims: FaDims) -> int:
 def fa_forward(Q, K, V, causal: bool, scale: float | None = None, O=None, L=None, stream=None, window: int = 0):
     """O, L = attention forward.  Optional preallocated O / L are written in place.
     ``window=W`` (causal only) lets each row see at most its last W keys."""
-    lib = load()
-    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
-        _check(t, n)
     dims = _dims_of(Q, K, V, causal, scale, window)
+    bf, f32 = torch.bfloat16, torch.float32
+    specs = [(Q, "Q", Q.shape, bf), (K, "K", K.shape, bf), (V, "V", V.shape, bf)]
+    if O is not None:
+        specs.append((O, "O", (dims.B, dims.Hq, dims.Tq, dims.dv), bf))
+    if L is not None:
+        specs.append((L, "L", (dims.B, dims.Hq, dims.Tq), f32))
+    _check_all(Q.device, specs)
     if O is None:
-        O = torch.empty(dims.B, dims.Hq, dims.Tq, dims.dv, dtype=torch.bfloat16, device=Q.device)
+        O = torch.empty(dims.B, dims.Hq, dims.Tq, dims.dv, dtype=bf, device=Q.device)
     if L is None:
-        L = torch.empty(dims.B, dims.Hq, dims.Tq, dtype=torch.float32, device=Q.device)
-    _check(O, "O")
-    _check(L, "L", torch.float32)
-    code = lib.fa_forward(ctypes.byref(dims), Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
-                          L.data_ptr(), _stream_ptr(stream))
+        L = torch.empty(dims.B, dims.Hq, dims.Tq, dtype=f32, device=Q.device)
+    lib = load()
+    with torch.cuda.device(Q.device):
+        code = lib.fa_forward(ctypes.byref(dims), Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                              L.data_ptr(), _stream_ptr(stream, Q.device))
     _raise(code, "fa_forward")
     return O, L
 
@@ -151,27 +171,40 @@ def fa_backward(Q, K, V, O, dO, L, causal: bool, scale: float | None = None, dQ=
     ``stages`` selects which of the three backward kernels to launch (see
     fa_backward_stages in include/fa.h); the default runs all of them.
     """
+    dims, dQ, dK, dV = _backward_operands(Q, K, V, O, dO, L, causal, scale, window, dQ, dK, dV)
     lib = load()
-    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (dO, "dO")):
-        _check(t, n)
-    _check(L, "L", torch.float32)
-    dims = _dims_of(Q, K, V, causal, scale, window)
-    dQ = torch.empty_like(Q) if dQ is None else dQ
-    dK = torch.empty_like(K) if dK is None else dK
-    dV = torch.empty_like(V) if dV is None else dV
-    for t, n in ((dQ, "dQ"), (dK, "dK"), (dV, "dV")):
-        _check(t, n)
     need = fa_backward_workspace_bytes(dims)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=Q.device)
+    elif not workspace.is_cuda or workspace.device != Q.device or not workspace.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous CUDA tensor on {Q.device}")
+    nbytes = workspace.numel() * workspace.element_size()
     args = (ctypes.byref(dims), Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), dO.data_ptr(),
-            L.data_ptr(), dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), workspace.data_ptr(), workspace.numel())
-    if stages == FA_BWD_ALL:
-        code = lib.fa_backward(*args, _stream_ptr(stream))
-    else:
-        code = lib.fa_backward_stages(*args, int(stages), _stream_ptr(stream))
+            L.data_ptr(), dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), workspace.data_ptr(), nbytes)
+    with torch.cuda.device(Q.device):
+        if stages == FA_BWD_ALL:
+            code = lib.fa_backward(*args, _stream_ptr(stream, Q.device))
+        else:
+            code = lib.fa_backward_stages(*args, int(stages), _stream_ptr(stream, Q.device))
     _raise(code, "fa_backward")
     return dQ, dK, dV
+
+
+def _backward_operands(Q, K, V, O, dO, L, causal, scale, window, dQ, dK, dV):
+    """Dims of a backward call, its gradient buffers (allocated when not given)
+    and the shape / dtype / device checks of all eleven tensors."""
+    dims = _dims_of(Q, K, V, causal, scale, window)
+    bf, f32 = torch.bfloat16, torch.float32
+    qv, rows = (dims.B, dims.Hq, dims.Tq, dims.dv), (dims.B, dims.Hq, dims.Tq)
+    specs = [(Q, "Q", Q.shape, bf), (K, "K", K.shape, bf), (V, "V", V.shape, bf),
+             (O, "O", qv, bf), (dO, "dO", qv, bf), (L, "L", rows, f32)]
+    specs += [(t, n, like.shape, bf) for t, n, like in ((dQ, "dQ", Q), (dK, "dK", K), (dV, "dV", V))
+              if t is not None]
+    _check_all(Q.device, specs)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    return dims, dQ, dK, dV
 
 
 def fa_backward_noalloc(Q, K, V, O, dO, L, causal: bool, scale: float | None = None, dQ=None, dK=None, dV=None,
@@ -180,19 +213,12 @@ def fa_backward_noalloc(Q, K, V, O, dO, L, causal: bool, scale: float | None = N
     memory: the library's fixed scratch array (FA_NOALLOC_SCRATCH_BYTES per
     GPU) is used instead.  Pass preallocated dQ / dK / dV to allocate nothing
     at all; calls that could overlap on the GPU must be ordered by the caller."""
+    dims, dQ, dK, dV = _backward_operands(Q, K, V, O, dO, L, causal, scale, window, dQ, dK, dV)
     lib = load()
-    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (dO, "dO")):
-        _check(t, n)
-    _check(L, "L", torch.float32)
-    dims = _dims_of(Q, K, V, causal, scale, window)
-    dQ = torch.empty_like(Q) if dQ is None else dQ
-    dK = torch.empty_like(K) if dK is None else dK
-    dV = torch.empty_like(V) if dV is None else dV
-    for t, n in ((dQ, "dQ"), (dK, "dK"), (dV, "dV")):
-        _check(t, n)
-    code = lib.fa_backward_noalloc(ctypes.byref(dims), Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
-                                   dO.data_ptr(), L.data_ptr(), dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(),
-                                   _stream_ptr(stream))
+    with torch.cuda.device(Q.device):
+        code = lib.fa_backward_noalloc(ctypes.byref(dims), Q.data_ptr(), K.data_ptr(), V.data_ptr(),
+                                       O.data_ptr(), dO.data_ptr(), L.data_ptr(), dQ.data_ptr(), dK.data_ptr(),
+                                       dV.data_ptr(), _stream_ptr(stream, Q.device))
     _raise(code, "fa_backward_noalloc")
     return dQ, dK, dV
 
