@@ -481,6 +481,14 @@ MUTANTS = {
     "dQ-uses-q": ("dq[c] += scale * dS * k[c];", "dq[c] += scale * dS * q[c];"),
     "window-off-by-one": ("- z.window + 1;", "- z.window;"),
     "dP-over-d-not-dv": ("for (int c = 0; c < dv; ++c) s += g[c] * v[c];", "for (int c = 0; c < d; ++c) s += g[c] * v[c];"),
+    "softmax-not-normalised": ("for (int64_t j = *j0; j < n; ++j) p[j] /= l;", ""),
+    "max-not-subtracted": ("p[j] = std::exp(p[j] - m);", "p[j] = std::exp(p[j]);"),
+    "scale-dropped-forward": ("s *= z.scale;", ""),
+    "D-without-p": ("Di += p[j] * s;", "Di += s;"),
+    "dV-without-p": ("dvv[c] += p[j] * g[c];", "dvv[c] += g[c];"),
+    "gqa-index-backward": ("const int64_t h = kvh * G + t / Tq,", "const int64_t h = kvh + (t / Tq) * Hkv,"),
+    "causal-top-left": ("int64_t e = i + (int64_t)(z.Tk - z.Tq) + 1;", "int64_t e = i + 1;"),
+    "window-ignores-offset": ("int64_t b = i + (int64_t)(z.Tk - z.Tq) - z.window + 1;", "int64_t b = i - z.window + 1;"),
 }
 
 
