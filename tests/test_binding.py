@@ -2,6 +2,11 @@
 pointers, so the binding must refuse every tensor whose shape, dtype, layout
 or device differs from what the kernels will index.  These run on the CPU and
 stop before anything reaches the library."""
+import os
+import subprocess
+import sys
+import textwrap
+
 import pytest
 import torch
 
@@ -74,3 +79,27 @@ def test_host_tensors_wrong_dtype_and_views_rejected():
     Qt = torch.zeros(1, 4, 64, 100, dtype=bf).transpose(2, 3)  # right shape, not contiguous
     with pytest.raises(ValueError, match="contiguous CUDA"):
         fa.fa_forward(Qt, K, V, False)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """With no built library and no compiler, loading raises instead of
+    falling back to anything else."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    child = textwrap.dedent(f"""
+        import sys
+        sys.path.insert(0, {root!r})
+        import tiled_attention_05_gb300.build as b
+        b.OUT_DIR = {str(tmp_path)!r}
+        b.LIB = {str(tmp_path / "libfa_gb300.so")!r}
+        import tiled_attention_05_gb300 as fa
+        try:
+            fa.load()
+        except Exception as e:
+            print("RAISED", type(e).__name__)
+        else:
+            print("LOADED")
+    """)
+    env = dict(os.environ, NVCC=str(tmp_path / "no-such-nvcc"))
+    r = subprocess.run([sys.executable, "-c", child], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert "RAISED" in r.stdout and "LOADED" not in r.stdout
