@@ -120,7 +120,8 @@ struct BwdParams {
   const float* delta;
   int* status;
   int Hq, Hkv, G, Tq, Tk, causal_off, q_tiles, kv_tiles;
-  int window;  // causal sliding window in keys, 0 = none
+  int sb_groups;  // (batch, kv head) groups per super-batch of the grid order; divides B * Hkv
+  int window;     // causal sliding window in keys, 0 = none
   long long Tq_pad;
   float scale_log2, scale;
 };
@@ -154,14 +155,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // One linear grid, key tile slowest: every group's tile 0 runs first, then
-  // tile 1, ...  Causal low key tiles see the most query rows, so this is
-  // heaviest-first over the whole grid, which keeps the tail short.  (Ordering
-  // by group instead keeps each group's dQ accumulator in L2 and cuts DRAM
-  // traffic about 4x, but its late heavy CTAs make the causal step ~12% longer.)
-  const int n_groups = (int)(gridDim.x / p.kv_tiles);
-  const int n = blockIdx.x / n_groups;  // key tile
-  const int bkv = blockIdx.x - n * n_groups;
+  // One linear grid in super-batches of sb_groups (batch, kv head) groups;
+  // within a super-batch the key tile is slowest: its groups' tile 0 runs
+  // first, then tile 1, ...  Causal low key tiles see the most query rows, so
+  // each super-batch runs heaviest-first and the next one's heavy CTAs fill
+  // the SMs its light ones free, which keeps the tail short.  Only a few
+  // groups' Q, dO and fp32 dQ accumulator are live at a time, so they stay in
+  // L2.  (One group at a time keeps even less live, but its late heavy CTAs
+  // make the causal step ~12% longer.)
+  const int per_sb = p.sb_groups * p.kv_tiles;
+  const int sb = blockIdx.x / per_sb;
+  const int in_sb = blockIdx.x - sb * per_sb;
+  const int n = in_sb / p.sb_groups;  // key tile
+  const int bkv = sb * p.sb_groups + (in_sb - n * p.sb_groups);
   const int b = bkv / p.Hkv, hk = bkv - b * p.Hkv;
   const int k0 = n * BN;
 
@@ -636,6 +642,18 @@ cudaError_t launch_main_dims(const fa::Problem& pr, const CUtensorMap* maps, con
   return launch_main_t<HD, HDV, true, false>(pr, maps, bp, stream);
 }
 
+// Groups per super-batch of fa_bwd_main's grid order: the smallest divisor of
+// the group count whose super-batch holds at least 1.5 CTAs per SM, so that
+// one super-batch fills the GPU with a heaviest-first queue of its own while
+// few groups' data is live in L2.  0 if the SM count cannot be read.
+int backward_super_batch(int n_groups, int kv_tiles) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess)
+    return 0;
+  return fa::super_batch_groups(n_groups, kv_tiles, sms);
+}
+
 inline int grid_for(long long work, int per_block) {
   long long g = (work + per_block - 1) / per_block;
   if (g > 152LL * 32) g = 152LL * 32;
@@ -723,6 +741,8 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
   bp.window = pr.causal ? pr.window : 0;
   bp.q_tiles = pr.q_tiles();
   bp.kv_tiles = pr.kv_tiles();
+  bp.sb_groups = backward_super_batch(pr.B * pr.Hkv, pr.kv_tiles());
+  if (bp.sb_groups < 1) return cudaErrorInvalidValue;
   bp.Tq_pad = pr.Tq_pad();
   bp.scale = pr.scale;
   bp.scale_log2 = pr.scale * 1.4426950408889634f;

@@ -40,6 +40,18 @@ cudaError_t launch_backward(const Problem& p, const void* Q, const void* K, cons
                             const void* dO, const float* L, void* dQ, void* dK, void* dV, void* workspace,
                             int stages, cudaStream_t stream, int* launches);
 
+// Groups per super-batch of the backward's grid order: the smallest divisor
+// S of n_groups with S * kv_tiles >= 1.5 * sms, searched up to four times the
+// least such S; n_groups (a single super-batch) when there is none.
+inline int super_batch_groups(int n_groups, int kv_tiles, int sms) {
+  if (n_groups < 1 || kv_tiles < 1) return n_groups;
+  const long long want = (3LL * sms + 1) / 2;
+  const long long s_min = want <= kv_tiles ? 1 : (want + kv_tiles - 1) / kv_tiles;
+  for (long long s = s_min; s < n_groups && s <= 4 * s_min; ++s)
+    if (n_groups % s == 0) return (int)s;
+  return n_groups;
+}
+
 // Workspace carve-up of fa_backward (byte offsets, 256-aligned).
 struct BwdWorkspace {
   size_t dq_acc, lse2, delta, total;
