@@ -4,6 +4,8 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "fa_internal.h"
 
@@ -114,6 +116,19 @@ int* device_status_word() {
     g_status_ptr[dev] = static_cast<int*>(p);
   }
   return g_status_ptr[dev];
+}
+
+cudaError_t allow_dynamic_smem(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count({kernel, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({kernel, dev});
+  return e;
 }
 
 }  // namespace fa

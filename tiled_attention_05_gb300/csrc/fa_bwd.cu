@@ -621,13 +621,8 @@ __global__ void fa_zero_words(uint32_t* p, size_t n) {
 template <int HD, int HDV, bool CAUSAL, bool WINDOW>
 cudaError_t launch_main_t(const fa::Problem& pr, const CUtensorMap* maps, const BwdParams& bp, cudaStream_t stream) {
   using C = BwdCfg<HD, HDV>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(fa_bwd_main<HD, HDV, CAUSAL, WINDOW>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = fa::allow_dynamic_smem(reinterpret_cast<const void*>(fa_bwd_main<HD, HDV, CAUSAL, WINDOW>), C::SMEM);
+  if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((long long)pr.B * pr.Hkv * pr.kv_tiles()));  // within int range (checked by the API)
   fa_bwd_main<HD, HDV, CAUSAL, WINDOW><<<grid, kThreads, C::SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
                                                                maps[6], bp);

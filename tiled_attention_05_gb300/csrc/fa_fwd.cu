@@ -440,13 +440,8 @@ template <int HD, int HDV, bool CAUSAL, bool WINDOW>
 cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mo, float* L, cudaStream_t stream) {
   using C = FwdCfg<HD, HDV>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<HD, HDV, CAUSAL, WINDOW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = fa::allow_dynamic_smem(reinterpret_cast<const void*>(fa_fwd_kernel<HD, HDV, CAUSAL, WINDOW>), C::SMEM);
+  if (e != cudaSuccess) return e;
   FwdParams p;
   p.L = L;
   p.status = fa::device_status_word();

@@ -32,6 +32,11 @@ bool encode_acc_f32(CUtensorMap* map, const void* base, int inner, long long row
 // Device status word of the current device (see fa_last_device_status).
 int* device_status_word();
 
+// Lets `kernel` use `bytes` of dynamic shared memory on the current device.
+// The attribute is per device, so it is set once for each (kernel, device)
+// pair; safe to call from several host threads.
+cudaError_t allow_dynamic_smem(const void* kernel, int bytes);
+
 // Launchers.  Each returns the first CUDA error it met and adds the number
 // of kernels it enqueued to *launches.
 cudaError_t launch_forward(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
