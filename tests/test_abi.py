@@ -103,3 +103,24 @@ def test_workspace_size_formula():
         want = up(up(up(rows * dd * 4) + rows * 4) + rows * 4)
         assert fa.fa_backward_workspace_bytes(d) == want
     assert fa.fa_backward_workspace_bytes(dims(Hq=3, Hkv=2)) == 0
+
+
+def test_binding_constants_match_the_header():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    enum = dict((k, int(v)) for k, v in re.findall(r"\b(FA_[A-Z_]+)\s*=\s*(\d+)", text))
+    for name in ("FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
+                 "FA_ERR_SCRATCH_TOO_SMALL", "FA_BWD_PRE", "FA_BWD_MAIN", "FA_BWD_CAST", "FA_BWD_ALL"):
+        assert getattr(fa, name) == enum[name], name
+    m = re.search(r"#define\s+FA_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m and fa.FA_NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+    # field order and types of fa_dims as the binding lays them out
+    body = re.search(r"typedef struct \{(.*?)\} fa_dims;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if decl:
+            typ, names = decl.split(None, 1)
+            fields += [(n.strip(), typ) for n in names.split(",")]
+    ctypes_of = {"int": ctypes.c_int, "float": ctypes.c_float}
+    assert [(n, ctypes_of[t]) for n, t in fields] == [(n, t) for n, t in fa.FaDims._fields_]
