@@ -65,6 +65,10 @@ def measured_traffic(workload: str):
 
 
 FLUSH_BYTES = 256 << 20
+# NVIDIA's nominal dense (no 2:4 sparsity) bf16 tensor peak of one GB300, in
+# TFLOP/s.  The roofline uses the measured cuBLAS figure; the fraction of this
+# nominal figure is reported beside it.
+NOMINAL_BF16_DENSE_TFLOPS = 2250.0
 
 
 def parse_args(argv=None):
@@ -117,31 +121,99 @@ def aggregate_throughput(units_per_rank: float, rank_seconds: float, world: int,
 
 
 # ---------------------------------------------------------------- clocks
-class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons every 50 ms.
+class _Nvml:
+    """Read-only NVML queries through ctypes (libnvidia-ml ships with the
+    driver): the SM clock, its maximum, the power draw and the active
+    clock-event (throttle) reasons of one GPU.  Nothing is ever set."""
 
-    It is started before the warm-up so that it is already sampling when the
-    timed region begins; each sample is stamped with the host wall clock on
-    arrival, and summary(t0, t1) keeps the samples taken inside [t0, t1].  A
-    timed region shorter than the sampling period gets the two samples around
-    it instead (both under load: warm-up before, end-to-end phase after), and
-    the summary says so."""
+    # nvmlClocksEventReason* bits (nvml.h)
+    SW_POWER_CAP, HW_SLOWDOWN, SW_THERMAL, HW_THERMAL = 0x4, 0x8, 0x20, 0x40
+    CLOCK_SM = 1
+
+    def __init__(self, index: int):
+        import ctypes
+
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.reasons_fn = fn
+        self.max_mhz = self._uint(self.lib.nvmlDeviceGetMaxClockInfo, self.CLOCK_SM)
+        self.index = index
+
+    def _uint(self, fn, *args):
+        v = self.ct.c_uint()
+        if fn(self.h, *args, self.ct.byref(v)) != 0:
+            raise OSError("NVML query failed")
+        return v.value
+
+    def line(self) -> str:
+        """One sample in the CSV form nvidia-smi prints for ClockSampler.FIELDS."""
+        sm = self._uint(self.lib.nvmlDeviceGetClockInfo, self.CLOCK_SM)
+        mw = self._uint(self.lib.nvmlDeviceGetPowerUsage)
+        r = self.ct.c_ulonglong()
+        if self.reasons_fn(self.h, self.ct.byref(r)) != 0:
+            raise OSError("NVML query failed")
+        bits = r.value
+        act = lambda b: "Active" if bits & b else "Not Active"  # noqa: E731
+        return (f"{self.index}, {sm}, {self.max_mhz}, {mw / 1000.0:.2f}, 0x{bits:016x}, {act(self.HW_SLOWDOWN)}, "
+                f"{act(self.HW_THERMAL)}, {act(self.SW_THERMAL)}, {act(self.SW_POWER_CAP)}")
+
+    def close(self):
+        try:
+            self.lib.nvmlShutdown()
+        except Exception:  # noqa: BLE001
+            pass
+
+
+class ClockSampler:
+    """Samples the SM clock, power and throttle reasons of one GPU.
+
+    It reads them through read-only NVML queries every 5 ms (falling back to
+    nvidia-smi at 10 ms when NVML cannot be loaded), so that even a timed
+    region of a few tens of milliseconds holds several samples.  It is started
+    before the warm-up so that it is already sampling when the timed region
+    begins; each sample is stamped with the host wall clock on arrival, and
+    summary(t0, t1) keeps the samples taken inside [t0, t1].  A timed region
+    shorter than the sampling period gets the two samples around it instead
+    (both under load: warm-up before, end-to-end phase after), and the summary
+    says so."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-    PERIOD_MS = 50
+    PERIOD_MS = 5
+    SMI_PERIOD_MS = 10
 
     def __init__(self, gpu_index: int):
         self.gpu_index = gpu_index
         self.proc = None
+        self.nvml = None
+        self.stop = threading.Event()
+        self.reader = None
+        self.source = "none"
         self.lines = []  # (host time of arrival, csv line)
 
     def __enter__(self):
         try:
+            self.nvml = _Nvml(self.gpu_index)
+            self.nvml.line()
+            self.source = f"NVML every {self.PERIOD_MS} ms"
+            self.reader = threading.Thread(target=self._poll, daemon=True)
+            self.reader.start()
+            return self
+        except (OSError, AttributeError):
+            self.nvml = None
+        try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", str(self.PERIOD_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.SMI_PERIOD_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = f"nvidia-smi every {self.SMI_PERIOD_MS} ms"
             self.reader = threading.Thread(target=self._read, daemon=True)
             self.reader.start()
         except OSError:
@@ -151,21 +223,34 @@ class ClockSampler:
     def wait_live(self, timeout_s: float = 3.0):
         """Block until the first sample has arrived (or the timeout passes)."""
         t_end = time.time() + timeout_s
-        while self.proc is not None and not self.lines and time.time() < t_end:
+        while (self.proc is not None or self.nvml is not None) and not self.lines and time.time() < t_end:
             time.sleep(0.01)
+
+    def _poll(self):
+        while not self.stop.is_set():
+            try:
+                self.lines.append((time.time(), self.nvml.line()))
+            except OSError:
+                pass
+            self.stop.wait(self.PERIOD_MS / 1000.0)
 
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
     def __exit__(self, *exc):
+        self.stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.reader is not None:
             self.reader.join(timeout=2)
+        if self.nvml is not None:
+            self.nvml.close()
+            self.nvml = None
 
     def summary(self, t0: float | None = None, t1: float | None = None):
         window = "whole run"
@@ -179,7 +264,7 @@ class ClockSampler:
                 after = [x for x in lines if x[0] > t1][:1]
                 lines = before + after
                 window = f"the samples just before and after the timed region ({(t1 - t0) * 1e3:.0f} ms, " \
-                         f"shorter than the {self.PERIOD_MS} ms sampling period)"
+                         f"shorter than the sampling period)"
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for _, ln in lines:
@@ -197,7 +282,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0, "window": window}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
-                "window": window}
+                "window": window, "source": self.source}
 
 
 # ---------------------------------------------------------------- CPU oracle legs
@@ -452,6 +537,7 @@ def run_ours(args, w):
                        "causal": w.causal, "window": w.window, "parallelism": "replicas" if world > 1 else "single",
                        "l2": "flushed before every timed step (256 MiB write)"},
             "pct_of_peak": 100.0 * value / peak,
+            "pct_of_nominal_peak": 100.0 * value / NOMINAL_BF16_DENSE_TFLOPS,
             "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
             "fwd_ms": statistics.mean(fwd_ms), "bwd_ms": statistics.mean(bwd_ms),
             "bwd_stage_ms": {"pre": statistics.mean(pre_ms), "main": statistics.mean(main_ms),

@@ -123,8 +123,12 @@ FA_API fa_status fa_backward_stages(const fa_dims* dims, const void* Q, const vo
  *    FA_NOALLOC_SCRATCH_BYTES is rejected with FA_ERR_SCRATCH_TOO_SMALL
  *    before anything is enqueued (use fa_backward for it).
  *  - Nothing is allocated or freed.  The first call on each device looks up
- *    the array's device address with that device current; make that first
- *    call before any stream capture on the device.
+ *    the array's device address with that device current and keeps it for
+ *    the life of the process; make that first call before any stream capture
+ *    on the device.  Resetting the device (cudaDeviceReset) after that first
+ *    call is not supported: the kept address would point into the destroyed
+ *    context.  (The device status word behind fa_last_device_status is kept
+ *    the same way.)
  *  - All calls on a device share the array.  Calls that may overlap on the
  *    GPU race on it; the caller must order them (e.g. one stream).  Stale
  *    contents from an earlier call are harmless: every part of the scratch the

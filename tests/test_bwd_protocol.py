@@ -18,11 +18,12 @@ A run fails on any of these:
   pass wrongly);
 - a read that sees another version than it needs.
 
-Two issue orders are checked. One is the kernel's: S^T(t+1) after dK(t) at
-d = 64 and after dQ(t) at d = 128, with dS^T packed into S^T's columns. The
-other issues S^T(t+1) right after dV(t) and packs dS^T over the dP^T columns
-already read. Planted protocol mistakes must each be caught, so the model is
-known to be able to fail.
+Two issue orders are checked. One is the kernel's: S^T(t+1) right after
+dV(t), with dS^T packed over the dP^T columns the elementwise warps have
+already read. The other is the kernel's earlier order, kept as a second
+known-good protocol: S^T(t+1) after dK(t) at d = 64 and after dQ(t) at
+d = 128, with dS^T packed into S^T's columns. Planted protocol mistakes must
+each be caught, so the model is known to be able to fail.
 """
 import random
 
@@ -237,7 +238,7 @@ def run(T, own_dq, new_order, seed, mutation=None):
 
 
 
-ORDERS = {"kernel": False, "S-after-dV": True}
+ORDERS = {"kernel": True, "earlier": False}
 
 
 @pytest.mark.parametrize("order", sorted(ORDERS))
@@ -249,9 +250,10 @@ def test_protocol_is_free_of_deadlock_aliasing_and_hazards(order, d):
 
 
 @pytest.mark.parametrize("mutation, order, d", [
-    ("dS-left-in-S-region", "S-after-dV", 128),   # S^T(t+1) would overwrite dS^T(t) before dK(t)
-    ("S-before-dV", "S-after-dV", 128),           # S^T(t+1) would overwrite P^T(t) before dV(t)
+    ("dS-left-in-S-region", "kernel", 128),       # S^T(t+1) would overwrite dS^T(t) before dK(t)
+    ("S-before-dV", "kernel", 128),               # S^T(t+1) would overwrite P^T(t) before dV(t)
     ("dP-skips-dQ-drain", "kernel", 128),         # dP^T(t+1) would overwrite dQ(t) before its drain
+    ("dP-skips-dQ-drain", "earlier", 128),
     ("dS-without-dP-wait", "kernel", 64),         # dS phase would read dP^T before it is written
 ])
 def test_planted_protocol_mistakes_are_caught(mutation, order, d):

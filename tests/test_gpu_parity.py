@@ -4,8 +4,8 @@ Small shapes are compared element by element in full (several 128-row tiles,
 ragged tails, GQA, causal with Tq == Tk, Tq < Tk and Tq > Tk, empty rows,
 causal sliding windows).  The named workloads run at full size in the same launch configuration
 the benchmark times; the oracle checks sampled forward rows of several heads
-and one complete GQA group (all of its query heads and rows, so dK and dV are
-complete) of the backward.
+and two complete GQA groups (all of their query heads and rows, so dK and dV
+are complete) of the backward.
 """
 from __future__ import annotations
 
@@ -263,38 +263,52 @@ def sample_rows(Tq):
     return sorted(r for r in rows if 0 <= r < Tq)
 
 
+# The five workloads whose tolerance is stated (max-abs 2e-2, rel-L2 1e-2, L
+# 1e-3): their full-size checks also hold every element with |ref| < 4 to the
+# bare max-abs bar (tests/parity.py says why not above).  The sliding-window
+# workload (added from "The Autograd Memory Trap", section "Assumptions and
+# Uncertainties") gets the general bar only.
+STATED = [n for n in WORKLOAD_ORDER if not n.startswith("swa_")]
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", WORKLOAD_ORDER)
 def test_workload_full_size(fa, name):
     w = WORKLOADS[name]
+    bare = name in STATED
     Q, K, V, dO = make_inputs(w)
     got = run_gpu(fa, Q, K, V, dO, w.causal, window=w.window)
     G = w.G
     # forward: sampled rows of the first and last head of the first and last batch
     heads = sorted({(0, 0), (0, w.Hq - 1), (w.B - 1, w.Hq // 2), (w.B - 1, w.Hq - 1)})
     rows = sample_rows(w.Tq)
-    fwd_err = {"O": {"max_abs": 0.0, "max_abs_beyond_rounding": 0.0, "rel_l2": 0.0}, "L": {"max_abs": 0.0}}
+    keys = ("max_abs", "max_abs_beyond_rounding", "rel_l2", "n_over_bare", "n_over_bare_below_4")
+    fwd_err = {"O": dict.fromkeys(keys, 0.0), "L": {"max_abs": 0.0}}
     for b, h in heads:
         kvh = h // G
         Qh, Kh, Vh = (oracle._f64(t) for t in (Q[b:b + 1, h:h + 1], K[b:b + 1, kvh:kvh + 1],
                                                  V[b:b + 1, kvh:kvh + 1]))
         for r in rows:
             O, L = oracle.forward(Qh, Kh, Vh, w.causal, rows=(r, r + 1), window=w.window)
-            eo = assert_close(f"O[{b},{h},{r}]", got["O"][b, h, r], O[0, 0, r])
+            eo = assert_close(f"O[{b},{h},{r}]", got["O"][b, h, r], O[0, 0, r], bare=bare)
             el = assert_L_close(f"L[{b},{h},{r}]", got["L"][b, h, r:r + 1], L[0, 0, r:r + 1])
-            for k in ("max_abs", "max_abs_beyond_rounding", "rel_l2"):
+            for k in keys:
                 fwd_err["O"][k] = max(fwd_err["O"][k], eo[k])
             fwd_err["L"]["max_abs"] = max(fwd_err["L"]["max_abs"], el["max_abs"])
-    # backward: one complete GQA group (the last one: last batch, last kv head).
-    b, kvh = w.B - 1, w.Hkv - 1
-    hs = slice(kvh * G, (kvh + 1) * G)
-    dQ, dK, dV, _ = oracle.backward(Q[b:b + 1, hs], K[b:b + 1, kvh:kvh + 1], V[b:b + 1, kvh:kvh + 1],
-                                    dO[b:b + 1, hs], w.causal, window=w.window)
-    report = {"workload": name}
-    report["dQ"] = assert_close("dQ(group)", got["dQ"][b:b + 1, hs], dQ)
-    report["dK"] = assert_close("dK(group)", got["dK"][b:b + 1, kvh:kvh + 1], dK)
-    report["dV"] = assert_close("dV(group)", got["dV"][b:b + 1, kvh:kvh + 1], dV)
-    report["O"], report["L"] = fwd_err["O"], fwd_err["L"]
+    # backward: two complete GQA groups (all their query heads and rows, so dK
+    # and dV are complete): the first (batch 0, kv head 0), which the backward
+    # grid runs in its first super-batch, and the last, in its last one.
+    report = {"workload": name, "O": fwd_err["O"], "L": fwd_err["L"]}
+    for b, kvh in sorted({(0, 0), (w.B - 1, w.Hkv - 1)}):
+        hs = slice(kvh * G, (kvh + 1) * G)
+        dQ, dK, dV, _ = oracle.backward(Q[b:b + 1, hs], K[b:b + 1, kvh:kvh + 1], V[b:b + 1, kvh:kvh + 1],
+                                        dO[b:b + 1, hs], w.causal, window=w.window)
+        tag = f"group b{b} kv{kvh}"
+        report[tag] = {
+            "dQ": assert_close(f"dQ({tag})", got["dQ"][b:b + 1, hs], dQ, bare=bare),
+            "dK": assert_close(f"dK({tag})", got["dK"][b:b + 1, kvh:kvh + 1], dK, bare=bare),
+            "dV": assert_close(f"dV({tag})", got["dV"][b:b + 1, kvh:kvh + 1], dV, bare=bare),
+        }
     print("PARITY", json.dumps(report))
     # the whole output is finite
     for n in ("O", "L", "dQ", "dK", "dV"):

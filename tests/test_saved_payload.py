@@ -131,8 +131,28 @@ def test_payload_table_shapes_and_closed_forms():
     assert 3 < rows[0][1] / rows[0][3] < 6 and 20 < rows[3][1] / rows[3][3] < 32
 
 
+def read_grad_golden():
+    """The gradient agreement the page prints (max abs difference of dQ, dK, dV
+    between the recomputing tiled path and the dense definition) and the
+    tolerance it asserts with."""
+    vals = {}
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "p1_grad_agreement.txt")):
+        if line.startswith("#") or not line.strip() or line.startswith("grad "):
+            continue
+        k, v = line.split()
+        vals[k] = float(v)
+    return vals
+
+
 def test_tiled_and_checkpointed_gradients_equal_dense():
-    """The page's equivalence check (random cotangent, float32)."""
+    """The page's equivalence check ("What Ordinary Autograd Saves", section
+    "The way out is recomputation, not a better forward pass"): seed 2, T = 128,
+    d = dv = 32, float32, a random cotangent.  The gradients of the tiled and the
+    checkpointed (recomputing) forward must match the dense definition within
+    the page's atol / rtol, and their max abs differences must sit at the same
+    float32 rounding level the page prints (4.8e-7, 4.2e-7, 4.8e-7; the exact
+    digits depend on the summation order, so within a factor of 4)."""
+    golden = read_grad_golden()
     torch.manual_seed(2)
     T, d = 128, 32
     Q, K, V = (torch.randn(T, d, requires_grad=True) for _ in range(3))
@@ -144,5 +164,7 @@ def test_tiled_and_checkpointed_gradients_equal_dense():
         (fn(Q, K, V) * up).sum().backward()
         grads[name] = [t.grad.clone() for t in (Q, K, V)]
     for other in ("ckpt", "tiled"):
-        for g, r in zip(grads[other], grads["dense"]):
-            torch.testing.assert_close(g, r, atol=1e-5, rtol=1e-5)
+        for gname, g, r in zip(("dQ", "dK", "dV"), grads[other], grads["dense"]):
+            torch.testing.assert_close(g, r, atol=golden["atol"], rtol=golden["rtol"])
+            diff = float((g - r).abs().max())
+            assert golden[gname] / 4 <= diff <= golden[gname] * 4, (other, gname, diff, golden[gname])

@@ -1,6 +1,7 @@
 // C ABI of the attention library: argument validation, TMA descriptor
 // encoding, the device status word and the workspace query.  The kernels and
 // their launchers live in fa_fwd.cu and fa_bwd.cu.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -14,6 +15,10 @@ namespace {
 __device__ int g_fa_status;  // 0, or a kernel's DEV_* code after a bounded wait gave up
 
 thread_local int t_last_launches = 0;
+
+#ifdef FA_TEST_HOOKS
+std::atomic<int> g_test_withhold{0};
+#endif
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -81,6 +86,10 @@ fa_status check_ptr(const void* p, long long elems) {
 }  // namespace
 
 namespace fa {
+
+#ifdef FA_TEST_HOOKS
+int test_withhold() { return g_test_withhold.load(); }
+#endif
 
 bool encode_rows_bf16(CUtensorMap* map, const void* base, int inner, int rows, long long outer) {
   EncodeTiledFn enc = encode_fn();
@@ -226,5 +235,12 @@ fa_status fa_last_device_status(void* stream) {
 }
 
 int fa_last_launch_count(void) { return t_last_launches; }
+
+#ifdef FA_TEST_HOOKS
+// Test build only (not declared in fa.h): 1 makes the forward's producer
+// withhold the Q tile, 2 the backward's producer withhold every dO tile, 0
+// restores normal loads.  Applies to launches made after the call.
+FA_API void fa_test_set_withhold(int what) { g_test_withhold.store(what); }
+#endif
 
 }  // extern "C"

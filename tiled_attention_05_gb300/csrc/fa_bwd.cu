@@ -25,26 +25,29 @@
 //   warp 0      TMA: K, V once; then Q_t (+ the tile's L and D slices by 1-D
 //               bulk copy) through a 2-deep ring and dO_t through one buffer.
 //   warp 1      tcgen05 issuer, per tile t:
-//                 S^T  = K Q_t^T        -> TMEM [0,128)      (key rows = lanes)
 //                 dP^T = V dO_t^T       -> TMEM [128,256)
 //                 dV  += P^T dO_t       A = P^T from TMEM (bf16, written over S^T)
-//                 dK  += dS^T Q_t       A = dS^T from TMEM (bf16, the other half of S^T)
+//                 S^T(t+1) = K Q_{t+1}^T -> TMEM [0,128)     (key rows = lanes)
+//                 dK  += dS^T Q_t       A = dS^T from TMEM (bf16, written over dP^T)
 //                 dQ_t = dS K           -> TMEM [128,128+d), or at d = 64 the free
-//                                        columns after dK; A = the same dS bytes
-//                                        read MN-major; B = K read MN-major
-//               with S^T(t+1) issued right after dK(t) (d = 64) or dQ(t) (d = 128),
-//               relying on in-order MMA execution rather than a wait.
+//                                        columns after dK; A = the dS bytes in
+//                                        shared memory read MN-major; B = K read MN-major
+//               relying on in-order MMA execution, not on waits, wherever a
+//               later MMA overwrites columns an earlier one reads.
 //   warps 4..11 two elementwise warpgroups (thread = key row = TMEM lane; group
 //               w owns query columns [64w, 64w+64)): P = exp2(S*scale*log2e - L2)
 //               with masks -> TMEM; dS = P * (dP - D) -> shared memory (for the
-//               dQ MMA) and, packed, into TMEM (for the dK MMA).
+//               dQ MMA) and, packed, into TMEM over dP^T (for the dK MMA).
 //               Epilogue: dV and dK*scale -> bf16 -> TMA store.
 //   warps 12..15 dQ warpgroup (thread = query row): each warp copies its 32
-//               rows of dQ_t out of TMEM two 32-column chunks at a time into its
-//               own 128B-swizzled fp32 staging slots and adds each chunk into
-//               the fp32 accumulator in global memory with one TMA bulk
-//               reduce-add (32 x 32 box); no cross-warp synchronisation.
-// TMEM columns: S^T/P [0,128), dP^T/dQ [128,256), dV [256,256+dv), dK [256+dv, 256+dv+d);
+//               rows of dQ_t out of TMEM into registers, releases the columns,
+//               then stages two 32-column chunks at a time in its own
+//               128B-swizzled fp32 slots and adds each chunk into the fp32
+//               accumulator in global memory with one TMA bulk reduce-add
+//               (32 x 32 box); no cross-warp synchronisation.  At d = 128 it
+//               takes registers from the producer / MMA warpgroup (setmaxnreg)
+//               to hold a whole dQ row.
+// TMEM columns: S^T/P^T [0,128), dP^T/dS^T/dQ [128,256), dV [256,256+dv), dK [256+dv, 256+dv+d);
 // at d = 64 dQ moves to [256+dv+d, 256+dv+2d).
 #include <cstdint>
 
@@ -58,6 +61,16 @@ namespace {
 constexpr int BM = fa::kTile;  // query rows per tile
 constexpr int BN = fa::kTile;  // keys per CTA
 constexpr int kThreads = 512;
+// Register split of fa_bwd_main at d = 128 (see the kernel): every thread
+// starts with kRegsLaunch; the producer / MMA warpgroup drops to kRegsLow and
+// the dQ warpgroup rises to kRegsHigh, the two elementwise warpgroups keep
+// kRegsLaunch.
+constexpr int kRegsLaunch = 65536 / kThreads;  // 128
+constexpr int kRegsLow = 80;
+constexpr int kRegsHigh = 2 * kRegsLaunch - kRegsLow;  // 192
+template <int HD>
+constexpr bool kSplitRegs = HD == 128;
+static_assert(kRegsLow % 8 == 0 && kRegsHigh % 8 == 0 && kRegsHigh <= 256, "setmaxnreg operands");
 
 // HD: head size of Q and K; HDV: head size of V, O and dO.
 template <int HD, int HDV>
@@ -124,6 +137,7 @@ struct BwdParams {
   int window;     // causal sliding window in keys, 0 = none
   long long Tq_pad;
   float scale_log2, scale;
+  int test_withhold_do;  // test build only: never issue the dO loads (the CTA's waits then time out)
 };
 
 // WINDOW (causal only): the sliding-window terms are compiled in only where
@@ -213,6 +227,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool run = (*abort_flag == 0) && T > 0;
+  // d = 128: the dQ warpgroup holds a whole 128-column dQ row in registers so
+  // that it can release dQ's TMEM columns before staging it; it takes the
+  // registers the producer / MMA warpgroup does not need (setmaxnreg at the
+  // top of both roles).  The launch gives every thread kRegsLaunch registers
+  // (the launcher checks this), and the shares add up to that total:
+  // kRegsLow + kRegsHigh = 2 * kRegsLaunch.
   const uint32_t T_S = tmem, T_DP = tmem + 128, T_DV = tmem + 256, T_DK = tmem + 256 + HDV;
   // dQ shares dP^T's columns unless there is room for columns of its own
   // (d = 64: dK ends at 384 or 448); then dP^T(t+1) need not wait for dQ(t)'s
@@ -221,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t T_DQ = kOwnDQ ? T_DK + HD : T_DP;
 
   if (warp < 4) {
+    if (kSplitRegs<HD>) setmaxnreg_dec<kRegsLow>();
     if (warp == 0 && lane == 0 && run) {
       // ---------------------------------------------------------- producer
       prefetch_tmap(&tmQ);
@@ -249,6 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < HDV / 64; ++cb) tma_prefetch_l2_3d(&tmdO, cb * 64, m * BM, bh);
         if (!mbar_wait(do_empty, (t & 1) ^ 1, abort_flag)) break;
+#ifdef FA_TEST_HOOKS
+        if (p.test_withhold_do) continue;
+#endif
         mbar_arrive_expect_tx(do_full, C::VO_TILE);
 #pragma unroll
         for (int cb = 0; cb < HDV / 64; ++cb)
@@ -277,14 +301,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                  desc_kmajor(q_base + (k >> 2) * (BM * 128) + (k & 3) * 32), id_sdp, k > 0 ? 1u : 0u);
         mma_commit(s_full);
       };
-      // Issue order per tile t: dP^T, dV, dK, then S^T(t+1) and dQ(t).  At d = 64
-      // S^T(t+1) goes first: the MMA queue is shallow, so behind dQ it would wait
-      // for dQ to execute.  At d = 128 dQ goes first: running it beside the next
-      // tile's elementwise P phase (whose shared loads SS MMAs slow down) costs
-      // more than it saves (measured).  S^T(t+1) overwrites the P^T / dS^T
-      // columns that dK reads; one thread's MMAs execute in issue order, so dK
-      // has read them by then.
-      constexpr bool kNextSFirst = HD == 64;
+      // Issue order per tile t: dP^T(t), dV(t), S^T(t+1), dK(t), dQ(t).  S^T(t+1)
+      // overwrites the P^T(t) columns dV(t) reads, and dQ(t) (d = 128) the dS^T(t)
+      // columns dK(t) reads; one thread's MMAs execute in issue order, so both
+      // have been read by then.  With S^T(t+1) right behind dV(t), the
+      // elementwise warps go from tile t's dS phase straight to tile t+1's P
+      // phase while dK(t), dQ(t) and dP^T(t+1) run.
       bool ok = mbar_wait(kv_full, 0, abort_flag) && mbar_wait(&q_full[0], 0, abort_flag);
       if (ok) {
         tc_fence_after();
@@ -293,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; ok && t < T; ++t) {
         const int st = t & 1;
         const uint32_t q_base = smem_u32(smem + C::OFF_Q + st * C::QK_TILE);
-        // dP^T shares its TMEM columns with dQ: the previous tile's dQ must be drained
+        // dP^T shares its TMEM columns with dQ (d = 128): the previous tile's dQ must be drained
         if (!mbar_wait(do_full, t & 1, abort_flag)) { ok = false; break; }
         if (!kOwnDQ && t > 0 && !mbar_wait(dq_empty, (t - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -304,40 +326,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(dp_full);
         if (!mbar_wait(p_ready, t & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        // P^T lives in TMEM as packed bf16: query columns [0,64) at TMEM columns
-        // [0,32), query columns [64,128) at [64,96) (each elementwise warpgroup
-        // overwrote its own half of S^T).
+        // P^T lives in TMEM as packed bf16 over S^T: query columns [0,64) at TMEM
+        // columns [0,32), query columns [64,128) at [64,96) (each elementwise
+        // warpgroup overwrote its own half of S^T).
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
           mma_ts(T_DV, T_S + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(do_base + k * 2048, BM * 128), id_dv,
                  (t > 0 || k > 0) ? 1u : 0u);
         mma_commit(do_empty);
-        // dS^T lives in TMEM too, packed into the other half of each group's
-        // S^T columns: query columns [0,64) at [32,64), [64,128) at [96,128).
-        // K steps 0, 1, 4, 5 (each warpgroup's first 32 query columns) go as
-        // soon as that half is written; 2, 3, 6, 7 once all of dS is.
+        if (t + 1 < T) {
+          if (!mbar_wait(&q_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          mma_s(t + 1);
+        }
+        // dS^T lives in TMEM as packed bf16 over dP^T, in the same column
+        // pattern as P^T: query columns [0,64) at [128,160), [64,128) at
+        // [192,224).  K steps 0, 1, 4, 5 (each warpgroup's first 32 query
+        // columns) go as soon as that half is written; 2, 3, 6, 7 once all of dS is.
         if (!mbar_wait(ds_half, t & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
           if ((k & 3) < 2)
-            mma_ts(T_DK, T_S + (k >> 2) * 64 + 32 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_dk,
+            mma_ts(T_DK, T_DP + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_dk,
                    (t > 0 || k > 0) ? 1u : 0u);
         if (!mbar_wait(ds_ready, t & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
           if ((k & 3) >= 2)
-            mma_ts(T_DK, T_S + (k >> 2) * 64 + 32 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_dk, 1u);
+            mma_ts(T_DK, T_DP + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_dk, 1u);
         mma_commit(&q_empty[st]);
-        auto next_s = [&]() -> bool {
-          if (t + 1 >= T) return true;
-          if (!mbar_wait(&q_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort_flag)) return false;
-          tc_fence_after();
-          mma_s(t + 1);
-          return true;
-        };
-        if (kNextSFirst && !next_s()) { ok = false; break; }
         if (kOwnDQ && t > 0) {  // dQ(t-1) drained from its columns
           if (!mbar_wait(dq_empty, (t - 1) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -347,7 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(T_DQ, desc_mnmajor(ds_base + k * 2048, BN * 128), desc_mnmajor(k_base + k * 2048, BN * 128), id_q,
                  k > 0 ? 1u : 0u);
         mma_commit(dq_full);
-        if (!kNextSFirst && !next_s()) { ok = false; break; }
       }
       mma_commit(acc_done);
       mma_commit(drain);
@@ -449,8 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             w[e + 1] = pack_bf16x2(f2_lo(s23), f2_hi(s23));
           }
           st_shared_v4(smem_u32(ds_blk + sw128_offset(r, ch * 4 + cc)), w[0], w[1], w[2], w[3]);
-          // packed dS^T of these 8 columns, for the dK MMA (A from TMEM)
-          tmem_st4(T_S + lane_base + wg * 64 + 32 + ch * 16 + cc * 4, w[0], w[1], w[2], w[3]);
+          // packed dS^T of these 8 columns, for the dK MMA (A from TMEM), over
+          // dP^T columns this thread has already read
+          tmem_st4(T_DP + lane_base + wg * 64 + ch * 16 + cc * 4, w[0], w[1], w[2], w[3]);
         }
         if (ch == 0) {  // first half of dS^T in TMEM: the dK MMA may start on it
           tmem_wait_st();
@@ -489,38 +508,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ warpgroup
-    // Each warp drains its own 32 query rows (its TMEM lanes): two 4 KB
-    // staging slots per warp (32 rows x 32 fp32, 128B-swizzled), one 32x32
-    // TMA reduce-add per slot; only warp-local ordering is needed.
+    if (kSplitRegs<HD>) setmaxnreg_inc<kRegsHigh>();
+    // Each warp drains its own 32 query rows (its TMEM lanes).  It copies all
+    // of its rows of dQ_t out of TMEM first and releases the columns at once
+    // (dP^T of the next tile waits for them at d = 128), then adds them into
+    // the fp32 accumulator two 32-column chunks at a time: two 4 KB staging
+    // slots per warp (32 rows x 32 fp32, 128B-swizzled), one 32x32 TMA
+    // reduce-add per slot; only warp-local ordering is needed.
     const int quad = warp & 3;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const bool leader = (lane == 0);
     uint8_t* wslot = smem + C::OFF_STG + quad * (2 * C::STG_SLOT);
-    constexpr int NCH = HD / 32;  // 32-column chunks per tile, drained two at a time
+    constexpr int NCH = HD / 32;  // 32-column chunks per tile
     bool ok = run;
     for (int t = 0; ok && t < T; ++t) {
       const int g = t / n_m, m = m_begin + (t - g * n_m);
       const int bh = b * p.Hq + hk * p.G + g;
       if (!__all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
+      uint32_t v[NCH][32];
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) tmem_ld32(T_DQ + lane_base + c * 32, v[c]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(dq_empty);  // all of dQ_t is out of TMEM: it may take dP_{t+1} (or dQ_{t+1})
 #pragma unroll
       for (int c = 0; c < NCH; c += 2) {
-        uint32_t v0[32], v1[32];
-        tmem_ld32(T_DQ + lane_base + c * 32, v0);
-        tmem_ld32(T_DQ + lane_base + (c + 1) * 32, v1);
-        tmem_wait_ld();
-        if (c + 2 >= NCH) {
-          tc_fence_before();
-          mbar_arrive(dq_empty);  // all of dQ_t is out of TMEM: it may take dP_{t+1} (or dQ_{t+1})
-        }
-        if (leader) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // both slots read
+        if (leader) bulk_wait_read0();  // both slots read by the previous reduce-adds
         __syncwarp();
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          st_shared_v4(smem_u32(wslot + sw128_offset(lane, q)), v0[4 * q], v0[4 * q + 1], v0[4 * q + 2],
-                       v0[4 * q + 3]);
-          st_shared_v4(smem_u32(wslot + C::STG_SLOT + sw128_offset(lane, q)), v1[4 * q], v1[4 * q + 1],
-                       v1[4 * q + 2], v1[4 * q + 3]);
+          st_shared_v4(smem_u32(wslot + sw128_offset(lane, q)), v[c][4 * q], v[c][4 * q + 1], v[c][4 * q + 2],
+                       v[c][4 * q + 3]);
+          st_shared_v4(smem_u32(wslot + C::STG_SLOT + sw128_offset(lane, q)), v[c + 1][4 * q], v[c + 1][4 * q + 1],
+                       v[c + 1][4 * q + 2], v[c + 1][4 * q + 3]);
         }
         fence_async_smem();
         __syncwarp();
@@ -621,8 +642,18 @@ __global__ void fa_zero_words(uint32_t* p, size_t n) {
 template <int HD, int HDV, bool CAUSAL, bool WINDOW>
 cudaError_t launch_main_t(const fa::Problem& pr, const CUtensorMap* maps, const BwdParams& bp, cudaStream_t stream) {
   using C = BwdCfg<HD, HDV>;
-  cudaError_t e = fa::allow_dynamic_smem(reinterpret_cast<const void*>(fa_bwd_main<HD, HDV, CAUSAL, WINDOW>), C::SMEM);
+  const void* fn = reinterpret_cast<const void*>(fa_bwd_main<HD, HDV, CAUSAL, WINDOW>);
+  cudaError_t e = fa::allow_dynamic_smem(fn, C::SMEM);
   if (e != cudaSuccess) return e;
+  if (kSplitRegs<HD>) {
+    // The register split only balances if every thread was launched with
+    // exactly kRegsLaunch registers; otherwise the dQ warpgroup's request
+    // could never be met, so refuse to launch.
+    cudaFuncAttributes fa_attr;
+    e = cudaFuncGetAttributes(&fa_attr, fn);
+    if (e != cudaSuccess) return e;
+    if (fa_attr.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+  }
   dim3 grid((unsigned)((long long)pr.B * pr.Hkv * pr.kv_tiles()));  // within int range (checked by the API)
   fa_bwd_main<HD, HDV, CAUSAL, WINDOW><<<grid, kThreads, C::SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
                                                                maps[6], bp);
@@ -741,6 +772,7 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
   bp.Tq_pad = pr.Tq_pad();
   bp.scale = pr.scale;
   bp.scale_log2 = pr.scale * 1.4426950408889634f;
+  bp.test_withhold_do = fa::test_withhold() == fa::kWithholdBwdDO;
   if (pr.d == 64)
     e = pr.dv == 64 ? launch_main_dims<64, 64>(pr, maps, bp, stream) : launch_main_dims<64, 128>(pr, maps, bp, stream);
   else

@@ -33,7 +33,6 @@
 // tile inside the union that one tile does not need is skipped by that tile's
 // MMAs and softmax.
 #include <cstdint>
-#include <cstdlib>
 
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
@@ -75,7 +74,7 @@ struct FwdParams {
   int window;      // causal sliding window in keys, 0 = none
   int kv_tiles;
   float scale_log2;  // scale * log2(e)
-  int test_withhold_q;  // failure-path test only: never issue the Q load (every wait then times out)
+  int test_withhold_q;  // test build only: never issue the Q load (every wait then times out)
 };
 
 // Key tiles [*beg, *end) that query rows [qa, qa+128) must visit (empty: 0, 0).
@@ -163,7 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      if (!p.test_withhold_q) {
+#ifdef FA_TEST_HOOKS
+      if (!p.test_withhold_q)
+#endif
+      {
         mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_BYTES);
 #pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb) {
@@ -217,7 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         v_last[s] = u;
       }
       // Every issued copy must land before the CTA releases its shared memory.
-      if (!p.test_withhold_q) mbar_wait_bounded(q_full, 0);
+#ifdef FA_TEST_HOOKS
+      if (!p.test_withhold_q)
+#endif
+        mbar_wait_bounded(q_full, 0);
 #pragma unroll
       for (int s = 0; s < NS; ++s) {
         if (k_last[s] >= 0) mbar_wait_bounded(&k_full[s], k_last[s] & 1);
@@ -454,11 +459,7 @@ cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUt
   p.window = pr.causal ? pr.window : 0;
   p.kv_tiles = pr.kv_tiles();
   p.scale_log2 = pr.scale * 1.4426950408889634f;
-  // Failure-path test switch (FA_TEST_WITHHOLD_Q=1): the producer withholds
-  // the Q tile, so the CTA's bounded waits expire and the kernel reports
-  // FA_ERR_TIMEOUT through the device status word instead of hanging.
-  const char* wq = getenv("FA_TEST_WITHHOLD_Q");
-  p.test_withhold_q = (wq && wq[0] == '1') ? 1 : 0;
+  p.test_withhold_q = fa::test_withhold() == fa::kWithholdFwdQ;
   dim3 grid(pr.B * pr.Hq, (pr.q_tiles() + 1) / 2);
   fa_fwd_kernel<HD, HDV, CAUSAL, WINDOW><<<grid, kThreads, C::SMEM, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();

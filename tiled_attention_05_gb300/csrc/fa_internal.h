@@ -9,6 +9,17 @@ namespace fa {
 
 constexpr int kTile = 128;  // rows of a query tile and of a key/value tile
 
+// Failure-path test hooks.  Only a separate test build of the library
+// (compiled with FA_TEST_HOOKS) can make a producer withhold one load, so that
+// a barrier is never completed and the kernel's bounded waits must expire;
+// the product build has neither the switch nor the code behind it.
+enum TestWithhold : int { kWithholdNone = 0, kWithholdFwdQ = 1, kWithholdBwdDO = 2 };
+#ifdef FA_TEST_HOOKS
+int test_withhold();
+#else
+constexpr int test_withhold() { return kWithholdNone; }
+#endif
+
 struct Problem {
   int B, Hq, Hkv, Tq, Tk, d, dv;  // d: Q/K head size, dv: V/O head size
   int causal;

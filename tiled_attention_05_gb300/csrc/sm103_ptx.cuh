@@ -269,6 +269,20 @@ __device__ __forceinline__ void red_add_v4(float* gptr, float a, float b, float 
                : "memory");
 }
 
+// ---------------------------------------------------------------- registers
+// Warpgroup-wide register reallocation: every warp of the warpgroup executes
+// the same instruction.  dec returns registers to the CTA's pool, inc waits
+// until the pool can grant its request, so the shares must add up to what the
+// CTA was launched with.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ float ex2(float x) {
   float y;
