@@ -24,6 +24,9 @@
 //                rescale the O row in TMEM when the max grows by more than 2^8
 //                (lazy rescaling, exact after the final normalisation);
 //                epilogue O / l -> bf16 -> TMA store, L -> global.
+//                The two softmax warpgroups take registers from the producer /
+//                MMA warpgroup (setmaxnreg), so that a whole score row stays in
+//                registers without spilling.
 // TMEM columns: S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,256+dv), O_B [384,384+dv).
 // Scores are kept in log2 units (scale * log2(e) folded into one FMA).
 //
@@ -44,6 +47,14 @@ namespace {
 constexpr int BM = fa::kTile;  // query rows per tile (two tiles per CTA)
 constexpr int BN = fa::kTile;  // keys per tile
 constexpr int kThreads = 384;
+// Register split: every thread starts with kRegsLaunch; the producer / MMA
+// warpgroup drops to kRegsLow and the two softmax warpgroups rise to
+// kRegsHigh (one score row of 128 fp32 values and its packed P in registers
+// without spilling).  kRegsLow + 2 * kRegsHigh = 3 * kRegsLaunch.
+constexpr int kRegsLaunch = 168;  // 65536 / 384 rounded down to a multiple of 8
+constexpr int kRegsLow = 88;
+constexpr int kRegsHigh = (3 * kRegsLaunch - kRegsLow) / 2;  // 208
+static_assert(kRegsLow + 2 * kRegsHigh == 3 * kRegsLaunch && kRegsHigh % 8 == 0, "setmaxnreg operands");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256 between rescales
 
 // HD: head size of Q and K (the score contraction); HDV: head size of V and O.
@@ -196,107 +207,111 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const bool run = (*abort_flag == 0) && nkv_max > 0;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && run) {
-      // Q and the first NS key/value tiles were issued during set-up.
-      int k_last[NS], v_last[NS];
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsLow>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0 && run) {
+        // Q and the first NS key/value tiles were issued during set-up.
+        int k_last[NS], v_last[NS];
 #pragma unroll
-      for (int s = 0; s < NS; ++s) k_last[s] = v_last[s] = s < nkv_max ? 0 : -1;
-      for (int jj = NS; jj < nkv_max; ++jj) {  // ring position jj holds key tile ub + jj
-        const int s = jj % NS, u = jj / NS, kv0 = (ub + jj) * BN;
-        if (!mbar_wait(&k_empty[s], (u & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&k_full[s], C::K_BYTES);
+        for (int s = 0; s < NS; ++s) k_last[s] = v_last[s] = s < nkv_max ? 0 : -1;
+        for (int jj = NS; jj < nkv_max; ++jj) {  // ring position jj holds key tile ub + jj
+          const int s = jj % NS, u = jj / NS, kv0 = (ub + jj) * BN;
+          if (!mbar_wait(&k_empty[s], (u & 1) ^ 1, abort_flag)) break;
+          mbar_arrive_expect_tx(&k_full[s], C::K_BYTES);
 #pragma unroll
-        for (int cb = 0; cb < HD / 64; ++cb)
-          tma_load_3d(smem + C::OFF_K + s * C::K_BYTES + cb * BN * 128, &tmK, &k_full[s], cb * 64, kv0, bkv);
-        k_last[s] = u;
-        if (!mbar_wait(&v_empty[s], (u & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&v_full[s], C::V_BYTES);
+          for (int cb = 0; cb < HD / 64; ++cb)
+            tma_load_3d(smem + C::OFF_K + s * C::K_BYTES + cb * BN * 128, &tmK, &k_full[s], cb * 64, kv0, bkv);
+          k_last[s] = u;
+          if (!mbar_wait(&v_empty[s], (u & 1) ^ 1, abort_flag)) break;
+          mbar_arrive_expect_tx(&v_full[s], C::V_BYTES);
 #pragma unroll
-        for (int cb = 0; cb < HDV / 64; ++cb)
-          tma_load_3d(smem + C::OFF_V + s * C::V_BYTES + cb * BN * 128, &tmV, &v_full[s], cb * 64, kv0, bkv);
-        v_last[s] = u;
-      }
-      // Every issued copy must land before the CTA releases its shared memory.
+          for (int cb = 0; cb < HDV / 64; ++cb)
+            tma_load_3d(smem + C::OFF_V + s * C::V_BYTES + cb * BN * 128, &tmV, &v_full[s], cb * 64, kv0, bkv);
+          v_last[s] = u;
+        }
+        // Every issued copy must land before the CTA releases its shared memory.
 #ifdef FA_TEST_HOOKS
-      if (!p.test_withhold_q)
+        if (!p.test_withhold_q)
 #endif
-        mbar_wait_bounded(q_full, 0);
+          mbar_wait_bounded(q_full, 0);
 #pragma unroll
-      for (int s = 0; s < NS; ++s) {
-        if (k_last[s] >= 0) mbar_wait_bounded(&k_full[s], k_last[s] & 1);
-        if (v_last[s] >= 0) mbar_wait_bounded(&v_full[s], v_last[s] & 1);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && run) {
-      constexpr uint32_t idS = idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t idPV = idesc_bf16(BM, HDV, 0, 1);
-      const uint32_t k_base = smem_u32(smem + C::OFF_K);
-      const uint32_t v_base = smem_u32(smem + C::OFF_V);
-      bool ok = mbar_wait(q_full, 0, abort_flag);
-      if (ok) tc_fence_after();
-      auto active = [&](int x, int j) { return j >= kb[x] && j < ke[x]; };
-      // S_X(j) = Q_X K_j^T into TMEM [128 X, 128 X + 128)
-      // Tile B's groups use the K_j / V_j tile A's groups have just waited
-      // for; re-waiting would only leave the tensor pipe idle for the round trip.
-      auto issue_s = [&](int x, int j) -> bool {
-        const int s = (j - ub) % NS;
-        if (!(x == 1 && active(0, j)) && !mbar_wait(&k_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t q_base = smem_u32(smem + C::OFF_Q + x * C::Q_BYTES);
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const uint64_t a = desc_kmajor(q_base + (k >> 2) * (BM * 128) + (k & 3) * 32);
-          const uint64_t bd = desc_kmajor(k_base + s * C::K_BYTES + (k >> 2) * (BN * 128) + (k & 3) * 32);
-          mma_ss(tmem + x * 128, a, bd, idS, k > 0 ? 1u : 0u);
-        }
-        mma_commit(&s_full[x]);
-        return true;
-      };
-      // O_X += P_X(j) V_j with P_X read from TMEM (packed bf16 over S_X)
-      auto issue_pv = [&](int x, int j) -> bool {
-        const int s = (j - ub) % NS;
-        // V_j has almost always landed: check it first, so that once P_X(j) is
-        // ready the MMAs go out without another round trip.
-        if (!(x == 1 && active(0, j)) && !mbar_wait(&v_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
-        if (!mbar_wait(&p_full[x], (j - kb[x]) & 1, abort_flag)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t bd = desc_mnmajor(v_base + s * C::V_BYTES + k * 2048, BN * 128);
-          mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, bd, idPV, (j > kb[x] || k > 0) ? 1u : 0u);
-        }
-        return true;
-      };
-      // A tile whose range starts at ub gets its first S up front; tile B, if
-      // it starts later, gets it in the loop below one step before its range.
-      if (ok && active(0, ub)) ok = issue_s(0, ub);
-      if (ok && active(1, ub)) ok = issue_s(1, ub);
-      if (ok) mma_commit(&k_empty[0]);
-      for (int j = ub; ok && j < ue; ++j) {
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          if (active(x, j)) {
-            if (!issue_pv(x, j)) { ok = false; break; }
-            if (x == 1 || !active(1, j)) mma_commit(&v_empty[(j - ub) % NS]);  // last reader of V_j
-          }
-          if (active(x, j + 1)) {
-            if (!issue_s(x, j + 1)) { ok = false; break; }
-            if (x == 1 || !active(1, j + 1)) mma_commit(&k_empty[(j + 1 - ub) % NS]);  // last reader of K_{j+1}
-          } else if (active(x, j)) {
-            mma_commit(&o_done[x]);
-          }
+        for (int s = 0; s < NS; ++s) {
+          if (k_last[s] >= 0) mbar_wait_bounded(&k_full[s], k_last[s] & 1);
+          if (v_last[s] >= 0) mbar_wait_bounded(&v_full[s], v_last[s] & 1);
         }
       }
-      // Let every MMA issued above finish before TMEM is released.
-      mma_commit(drain);
-      mbar_wait_bounded(drain, 0);
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0 && run) {
+        constexpr uint32_t idS = idesc_bf16(BM, BN, 0, 0);
+        constexpr uint32_t idPV = idesc_bf16(BM, HDV, 0, 1);
+        const uint32_t k_base = smem_u32(smem + C::OFF_K);
+        const uint32_t v_base = smem_u32(smem + C::OFF_V);
+        bool ok = mbar_wait(q_full, 0, abort_flag);
+        if (ok) tc_fence_after();
+        auto active = [&](int x, int j) { return j >= kb[x] && j < ke[x]; };
+        // S_X(j) = Q_X K_j^T into TMEM [128 X, 128 X + 128)
+        // Tile B's groups use the K_j / V_j tile A's groups have just waited
+        // for; re-waiting would only leave the tensor pipe idle for the round trip.
+        auto issue_s = [&](int x, int j) -> bool {
+          const int s = (j - ub) % NS;
+          if (!(x == 1 && active(0, j)) && !mbar_wait(&k_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t q_base = smem_u32(smem + C::OFF_Q + x * C::Q_BYTES);
+#pragma unroll
+          for (int k = 0; k < HD / 16; ++k) {
+            const uint64_t a = desc_kmajor(q_base + (k >> 2) * (BM * 128) + (k & 3) * 32);
+            const uint64_t bd = desc_kmajor(k_base + s * C::K_BYTES + (k >> 2) * (BN * 128) + (k & 3) * 32);
+            mma_ss(tmem + x * 128, a, bd, idS, k > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[x]);
+          return true;
+        };
+        // O_X += P_X(j) V_j with P_X read from TMEM (packed bf16 over S_X)
+        auto issue_pv = [&](int x, int j) -> bool {
+          const int s = (j - ub) % NS;
+          // V_j has almost always landed: check it first, so that once P_X(j) is
+          // ready the MMAs go out without another round trip.
+          if (!(x == 1 && active(0, j)) && !mbar_wait(&v_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
+          if (!mbar_wait(&p_full[x], (j - kb[x]) & 1, abort_flag)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k) {
+            const uint64_t bd = desc_mnmajor(v_base + s * C::V_BYTES + k * 2048, BN * 128);
+            mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, bd, idPV, (j > kb[x] || k > 0) ? 1u : 0u);
+          }
+          return true;
+        };
+        // A tile whose range starts at ub gets its first S up front; tile B, if
+        // it starts later, gets it in the loop below one step before its range.
+        if (ok && active(0, ub)) ok = issue_s(0, ub);
+        if (ok && active(1, ub)) ok = issue_s(1, ub);
+        if (ok) mma_commit(&k_empty[0]);
+        for (int j = ub; ok && j < ue; ++j) {
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (active(x, j)) {
+              if (!issue_pv(x, j)) { ok = false; break; }
+              if (x == 1 || !active(1, j)) mma_commit(&v_empty[(j - ub) % NS]);  // last reader of V_j
+            }
+            if (active(x, j + 1)) {
+              if (!issue_s(x, j + 1)) { ok = false; break; }
+              if (x == 1 || !active(1, j + 1)) mma_commit(&k_empty[(j + 1 - ub) % NS]);  // last reader of K_{j+1}
+            } else if (active(x, j)) {
+              mma_commit(&o_done[x]);
+            }
+          }
+        }
+        // Let every MMA issued above finish before TMEM is released.
+        mma_commit(drain);
+        mbar_wait_bounded(drain, 0);
+      }
     }
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------------------------------------ softmax + epilogue of tile x
+    setmaxnreg_inc<kRegsHigh>();
     const int x = (warp - 4) >> 2;
     const int kbx = x ? kb[1] : kb[0];  // first key tile of this tile's range
     const int nkv = (x ? ke[1] : ke[0]) - kbx;
@@ -445,8 +460,16 @@ template <int HD, int HDV, bool CAUSAL, bool WINDOW>
 cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mo, float* L, cudaStream_t stream) {
   using C = FwdCfg<HD, HDV>;
-  cudaError_t e = fa::allow_dynamic_smem(reinterpret_cast<const void*>(fa_fwd_kernel<HD, HDV, CAUSAL, WINDOW>), C::SMEM);
+  const void* fn = reinterpret_cast<const void*>(fa_fwd_kernel<HD, HDV, CAUSAL, WINDOW>);
+  cudaError_t e = fa::allow_dynamic_smem(fn, C::SMEM);
   if (e != cudaSuccess) return e;
+  // The register split only balances if every thread was launched with
+  // exactly kRegsLaunch registers; otherwise the softmax warpgroups' request
+  // could never be met, so refuse to launch.
+  cudaFuncAttributes fa_attr;
+  e = cudaFuncGetAttributes(&fa_attr, fn);
+  if (e != cudaSuccess) return e;
+  if (fa_attr.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   FwdParams p;
   p.L = L;
   p.status = fa::device_status_word();
