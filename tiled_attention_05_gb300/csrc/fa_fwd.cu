@@ -72,7 +72,7 @@ struct FwdCfg {
   static constexpr int OFF_O = O_IN_Q ? OFF_Q : OFF_V + NS * V_BYTES;  // [2]
   static constexpr int O_STRIDE = O_IN_Q ? Q_BYTES : O_BYTES;
   static constexpr int OFF_BAR = O_IN_Q ? OFF_V + NS * V_BYTES : OFF_O + 2 * O_BYTES;
-  static constexpr int NBAR = 1 + 4 * NS + 2 + 2 + 2 + 1;
+  static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 2 + 1;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -123,10 +123,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* k_full = q_full + 1;
-  uint64_t* k_empty = k_full + NS;
-  uint64_t* v_full = k_empty + NS;
-  uint64_t* v_empty = v_full + NS;
+  // One "full" barrier per ring slot covers both K_j and V_j, so the MMA
+  // thread checks a key tile once; K and V are released separately (K after
+  // the last S that reads it, V after the last P.V), so K_{j+NS} can load
+  // before V_j's readers are done.
+  uint64_t* kv_full = q_full + 1;
+  uint64_t* k_empty = kv_full + NS;
+  uint64_t* v_empty = k_empty + NS;
   uint64_t* s_full = v_empty + NS;  // [2] per tile
   uint64_t* p_full = s_full + 2;    // [2]
   uint64_t* o_done = p_full + 2;    // [2]
@@ -154,9 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;  // swizzled tiles need 1024 B alignment
     mbar_init(q_full, 1);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&k_full[s], 1);
+      mbar_init(&kv_full[s], 1);
       mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
@@ -186,14 +188,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int jj = 0; jj < NS && jj < nkv_max; ++jj) {
         const int kv0 = (ub + jj) * BN;
-        mbar_arrive_expect_tx(&k_full[jj], C::K_BYTES);
+        mbar_arrive_expect_tx(&kv_full[jj], C::K_BYTES + C::V_BYTES);
 #pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
-          tma_load_3d(smem + C::OFF_K + jj * C::K_BYTES + cb * BN * 128, &tmK, &k_full[jj], cb * 64, kv0, bkv);
-        mbar_arrive_expect_tx(&v_full[jj], C::V_BYTES);
+          tma_load_3d(smem + C::OFF_K + jj * C::K_BYTES + cb * BN * 128, &tmK, &kv_full[jj], cb * 64, kv0, bkv);
 #pragma unroll
         for (int cb = 0; cb < HDV / 64; ++cb)
-          tma_load_3d(smem + C::OFF_V + jj * C::V_BYTES + cb * BN * 128, &tmV, &v_full[jj], cb * 64, kv0, bkv);
+          tma_load_3d(smem + C::OFF_V + jj * C::V_BYTES + cb * BN * 128, &tmV, &kv_full[jj], cb * 64, kv0, bkv);
       }
     }
   }
@@ -213,23 +214,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------ producer
       if (lane == 0 && run) {
         // Q and the first NS key/value tiles were issued during set-up.
-        int k_last[NS], v_last[NS];
+        int kv_last[NS];  // last ring pass whose K and V loads were both issued, per slot
+        bool half = false;  // a K load was issued whose V load was not (abort in between)
 #pragma unroll
-        for (int s = 0; s < NS; ++s) k_last[s] = v_last[s] = s < nkv_max ? 0 : -1;
+        for (int s = 0; s < NS; ++s) kv_last[s] = s < nkv_max ? 0 : -1;
         for (int jj = NS; jj < nkv_max; ++jj) {  // ring position jj holds key tile ub + jj
           const int s = jj % NS, u = jj / NS, kv0 = (ub + jj) * BN;
           if (!mbar_wait(&k_empty[s], (u & 1) ^ 1, abort_flag)) break;
-          mbar_arrive_expect_tx(&k_full[s], C::K_BYTES);
+          mbar_arrive_expect_tx(&kv_full[s], C::K_BYTES + C::V_BYTES);
 #pragma unroll
           for (int cb = 0; cb < HD / 64; ++cb)
-            tma_load_3d(smem + C::OFF_K + s * C::K_BYTES + cb * BN * 128, &tmK, &k_full[s], cb * 64, kv0, bkv);
-          k_last[s] = u;
+            tma_load_3d(smem + C::OFF_K + s * C::K_BYTES + cb * BN * 128, &tmK, &kv_full[s], cb * 64, kv0, bkv);
+          half = true;
           if (!mbar_wait(&v_empty[s], (u & 1) ^ 1, abort_flag)) break;
-          mbar_arrive_expect_tx(&v_full[s], C::V_BYTES);
 #pragma unroll
           for (int cb = 0; cb < HDV / 64; ++cb)
-            tma_load_3d(smem + C::OFF_V + s * C::V_BYTES + cb * BN * 128, &tmV, &v_full[s], cb * 64, kv0, bkv);
-          v_last[s] = u;
+            tma_load_3d(smem + C::OFF_V + s * C::V_BYTES + cb * BN * 128, &tmV, &kv_full[s], cb * 64, kv0, bkv);
+          half = false;
+          kv_last[s] = u;
         }
         // Every issued copy must land before the CTA releases its shared memory.
 #ifdef FA_TEST_HOOKS
@@ -237,9 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
           mbar_wait_bounded(q_full, 0);
 #pragma unroll
-        for (int s = 0; s < NS; ++s) {
-          if (k_last[s] >= 0) mbar_wait_bounded(&k_full[s], k_last[s] & 1);
-          if (v_last[s] >= 0) mbar_wait_bounded(&v_full[s], v_last[s] & 1);
+        for (int s = 0; s < NS; ++s)
+          if (kv_last[s] >= 0) mbar_wait_bounded(&kv_full[s], kv_last[s] & 1);
+        // A K load whose V never followed leaves its barrier short of bytes:
+        // give the copy in flight time to land before the CTA exits.
+        if (half) {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 1000000ull) {
+          }
         }
       }
     } else if (warp == 1) {
@@ -257,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // for; re-waiting would only leave the tensor pipe idle for the round trip.
         auto issue_s = [&](int x, int j) -> bool {
           const int s = (j - ub) % NS;
-          if (!(x == 1 && active(0, j)) && !mbar_wait(&k_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
+          if (!(x == 1 && active(0, j)) && !mbar_wait(&kv_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
           tc_fence_after();
           const uint32_t q_base = smem_u32(smem + C::OFF_Q + x * C::Q_BYTES);
 #pragma unroll
@@ -272,9 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O_X += P_X(j) V_j with P_X read from TMEM (packed bf16 over S_X)
         auto issue_pv = [&](int x, int j) -> bool {
           const int s = (j - ub) % NS;
-          // V_j has almost always landed: check it first, so that once P_X(j) is
-          // ready the MMAs go out without another round trip.
-          if (!(x == 1 && active(0, j)) && !mbar_wait(&v_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
+          // V_j landed with K_j: the S(j) MMA before this P.V waited for both.
           if (!mbar_wait(&p_full[x], (j - kb[x]) & 1, abort_flag)) return false;
           tc_fence_after();
 #pragma unroll
