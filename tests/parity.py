@@ -17,6 +17,15 @@ the products (P, dS and the inputs) add their own relative error of about
 The count of elements past the bare 2e-2 over the whole tensor (n_over_bare)
 and among |ref| < 4 (n_over_bare_below_4) are reported beside it.  The rel-L2
 bar and the L bar are applied unchanged everywhere.
+
+The stated bars were set for the stated workloads, whose gradients stay below
+about 10 in magnitude.  The seeded random-shape sweep also draws problems
+with a handful of keys and hundreds of query rows, where dK and dV reach
+10-20: there a bf16 operand (P, dS) carries a relative error of 2^-9 into
+every term of a sum over all those rows, and a CPU emulation of exactly that
+arithmetic lands 0.05 from the float64 result on one such shape.  For the
+sweep only (``magnitude=True``) the element-wise bar adds one bf16 step at the
+tensor's largest value, 2^-8 * max|ref|.
 """
 from __future__ import annotations
 
@@ -60,14 +69,16 @@ def errors(gpu, ref) -> dict:
     }
 
 
-def assert_close(name, gpu, ref, rel_l2=REL_L2, bare=False):
+def assert_close(name, gpu, ref, rel_l2=REL_L2, bare=False, magnitude=False):
     """The bars on a bf16 output (see the module docstring): element-wise
     max-abs 2e-2 beyond half a bf16 ulp of the reference (and, with
-    ``bare=True``, the bare 2e-2 wherever |ref| < 4), and rel-L2 1e-2."""
+    ``bare=True``, the bare 2e-2 wherever |ref| < 4; with ``magnitude=True``,
+    2^-8 * max|ref| more), and rel-L2 1e-2."""
     e = errors(gpu, ref)
     assert e["finite_ok"], f"{name}: non-finite mismatch"
-    assert e["max_abs_beyond_rounding"] <= MAX_ABS, \
-        f"{name}: max-abs beyond bf16 output rounding {e['max_abs_beyond_rounding']:.3e} > {MAX_ABS} ({e})"
+    bar = MAX_ABS + (2.0 ** -8 * e["max_ref"] if magnitude else 0.0)
+    assert e["max_abs_beyond_rounding"] <= bar, \
+        f"{name}: max-abs beyond bf16 output rounding {e['max_abs_beyond_rounding']:.3e} > {bar:.3e} ({e})"
     if bare:
         assert e["n_over_bare_below_4"] == 0, \
             f"{name}: {e['n_over_bare_below_4']} elements with |ref| < 4 past the bare max-abs {MAX_ABS} ({e})"

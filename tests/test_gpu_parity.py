@@ -372,3 +372,53 @@ def test_every_output_element_is_written(fa, shape):
     assert_L_close("L", L.cpu(), Lr)
     for n, g, r in (("dQ", dQ, dQr), ("dK", dK, dKr), ("dV", dV, dVr)):
         assert_close(n, g.cpu(), r)
+
+
+def test_every_element_over_two_super_batches(fa):
+    """Every element of O, L, dQ, dK and dV against the oracle at a shape whose
+    backward grid runs its 16 (batch, kv head) groups in two super-batches of
+    8 on a 152-SM GB300 (32 key tiles each, ragged last tile): the grid order,
+    the fp32 dQ reduction across 32 key-tile CTAs and every group's dK and dV
+    are checked in full, not sampled."""
+    B, Hq, Hkv, T, d = 2, 32, 8, 4000, 128
+    Q, K, V, dO = make_custom(B, Hq, Hkv, T, T, d, True, seed=4000)
+    got = run_gpu(fa, Q, K, V, dO, True)
+    O, L = oracle.forward(Q, K, V, True)
+    dQ, dK, dV, _ = oracle.backward(Q, K, V, dO, True)
+    assert_close("O", got["O"], O)
+    assert_L_close("L", got["L"], L)
+    for n, ref in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+        assert_close(n, got[n], ref)
+
+
+def random_shapes(n, seed):
+    """Seeded random problems: GQA ratio, ragged lengths on both sides, head
+    sizes, causal or not, and causal sliding windows of random width."""
+    rnd = np.random.default_rng(seed)
+    shapes = []
+    for i in range(n):
+        Hkv = int(rnd.choice([1, 2, 4]))
+        G = int(rnd.choice([1, 2, 4]))
+        Tq, Tk = (int(x) for x in rnd.integers(1, 700, size=2))
+        d, dv = (int(x) for x in rnd.choice([64, 128], size=2))
+        kind = i % 3  # full, causal, causal with a window
+        W = int(rnd.integers(1, Tk + 1)) if kind == 2 else 0
+        shapes.append((int(rnd.integers(1, 3)), Hkv * G, Hkv, Tq, Tk, d, dv, kind > 0, W))
+    return shapes
+
+
+@pytest.mark.parametrize("shape", random_shapes(16, seed=2026), ids=lambda s: "x".join(map(str, s[:7])) +
+                         ("c" if s[7] else "") + (f"w{s[8]}" if s[8] else ""))
+def test_random_shapes_full_parity(fa, shape):
+    """Every element, on seeded random shapes.  Some draw only a few keys for
+    hundreds of rows, so their gradients are large: the element-wise bar gets
+    the magnitude term of tests/parity.py (rel-L2 stays 1e-2)."""
+    B, Hq, Hkv, Tq, Tk, d, dv, causal, W = shape
+    Q, K, V, dO = make_custom(B, Hq, Hkv, Tq, Tk, d, causal, seed=Tq * 1000 + Tk, dv=dv)
+    got = run_gpu(fa, Q, K, V, dO, causal, window=W)
+    O, L = oracle.forward(Q, K, V, causal, window=W)
+    dQ, dK, dV, _ = oracle.backward(Q, K, V, dO, causal, window=W)
+    assert_close("O", got["O"], O, magnitude=True)
+    assert_L_close("L", got["L"], L)
+    for n, ref in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+        assert_close(n, got[n], ref, magnitude=True)
