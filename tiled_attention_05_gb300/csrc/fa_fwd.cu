@@ -7,9 +7,14 @@
 // output when the maximum moves; normalise once at the end and emit
 // L = m + log(l) beside O.  Nothing of size Tq x Tk is ever stored.
 //
-// GB300 mapping: one CTA = two 128-row query tiles (A and B) of one
-// (batch, head), sharing every K/V tile it loads.
-//   warp 0       TMA producer: Q_A and Q_B once, then K_j / V_j through NS-deep rings.
+// GB300 mapping: a persistent grid of one CTA per SM.  A work item is two
+// 128-row query tiles (A and B) of one (batch, head), sharing every K/V tile
+// the CTA loads for it; each CTA walks its items (heaviest causal rows first,
+// in a snake order over the CTAs so that their totals even out) and starts
+// the next item's loads and first MMAs while the current one finishes.
+//   warp 0       TMA producer: Q_A, Q_B per item (each as soon as the last
+//                S of the previous item's tile has read its buffer), then the
+//                item's K_j / V_j through NS-deep rings that run on across items.
 //   warp 1       tcgen05 issuer.  Per key tile j it issues, in this order,
 //                  O_A += P_A(j) V_j,  S_A(j+1) = Q_A K_{j+1}^T,
 //                  O_B += P_B(j) V_j,  S_B(j+1) = Q_B K_{j+1}^T,
@@ -17,13 +22,18 @@
 //                pipe runs the other tile's two MMAs (ping-pong).  P is read
 //                straight from TMEM (A operand); the MMAs of one thread execute
 //                in issue order, so S_X(j+1) overwrites P_X(j) only after the
-//                P.V that reads it.
+//                P.V that reads it.  An item's first S MMAs follow the previous
+//                item's last P.V at once, while the softmax warpgroups write
+//                that item's output.
 //   warps 4..7   softmax of tile A, warps 8..11 softmax of tile B (thread =
 //                query row = TMEM lane): load the score row, mask, row max,
 //                exp2, row sum, write P as packed bf16 over the scores in TMEM;
 //                rescale the O row in TMEM when the max grows by more than 2^8
 //                (lazy rescaling, exact after the final normalisation);
-//                epilogue O / l -> bf16 -> TMA store, L -> global.
+//                epilogue O / l -> bf16 -> global (each thread its row), L -> global.
+//                The next item's first P.V into O_X waits for this warpgroup's
+//                first P of that item, which it writes only after its epilogue
+//                has read O_X out of TMEM.
 //                The two softmax warpgroups take registers from the producer /
 //                MMA warpgroup (setmaxnreg), so that a whole score row stays in
 //                registers without spilling.
@@ -34,7 +44,8 @@
 // the diagonal; with a sliding window of W keys also from the first row's
 // window start on).  The CTA loads the union of the two ranges once; a key
 // tile inside the union that one tile does not need is skipped by that tile's
-// MMAs and softmax.
+// MMAs and softmax.  Every barrier phase (and ring position) is counted from
+// the start of the CTA, not of the item.
 #include <cstdint>
 
 #include "fa_internal.h"
@@ -44,7 +55,7 @@ using namespace fa_ptx;
 
 namespace {
 
-constexpr int BM = fa::kTile;  // query rows per tile (two tiles per CTA)
+constexpr int BM = fa::kTile;  // query rows per tile (two tiles per work item)
 constexpr int BN = fa::kTile;  // keys per tile
 constexpr int kThreads = 384;
 // Register split: every thread starts with kRegsLaunch; the producer / MMA
@@ -64,28 +75,28 @@ struct FwdCfg {
   static constexpr int Q_BYTES = BM * HD * 2;
   static constexpr int K_BYTES = BN * HD * 2;
   static constexpr int V_BYTES = BN * HDV * 2;
-  static constexpr int O_BYTES = BM * HDV * 2;  // one tile's bf16 O, staged for its TMA store
-  static constexpr bool O_IN_Q = O_BYTES <= Q_BYTES;  // O staged in the tile's own (idle) Q buffer
   static constexpr int OFF_Q = 0;  // [2]: tile A, tile B
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NS * K_BYTES;
-  static constexpr int OFF_O = O_IN_Q ? OFF_Q : OFF_V + NS * V_BYTES;  // [2]
-  static constexpr int O_STRIDE = O_IN_Q ? Q_BYTES : O_BYTES;
-  static constexpr int OFF_BAR = O_IN_Q ? OFF_V + NS * V_BYTES : OFF_O + 2 * O_BYTES;
-  static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 2 + 1;
+  static constexpr int OFF_BAR = OFF_V + NS * V_BYTES;
+  static constexpr int NBAR = 2 + 2 + 3 * NS + 2 + 2 + 2 + 1;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct FwdParams {
+  uint16_t* O;  // bf16 [B, Hq, Tq, dv]
   float* L;
   int* status;
   int Hq, Hkv, G, Tq, Tk;
   int causal_off;  // Tk - Tq
   int window;      // causal sliding window in keys, 0 = none
   int kv_tiles;
+  int n_bh;            // B * Hq
+  int n_pairs;         // query-tile pairs per (batch, head)
+  long long n_items;   // n_bh * n_pairs
   float scale_log2;  // scale * log2(e)
-  int test_withhold_q;  // test build only: never issue the Q load (every wait then times out)
+  int test_withhold_q;  // test build only: never issue the Q loads (every wait then times out)
 };
 
 // Key tiles [*beg, *end) that query rows [qa, qa+128) must visit (empty: 0, 0).
@@ -111,23 +122,55 @@ __device__ __forceinline__ void kv_range_for(const FwdParams& p, int qa, int* be
   }
 }
 
+// One work item: query tiles A = [q0, q0 + 128) and B = [q0 + 128, q0 + 256)
+// of (batch, head) bh, and the key tiles each must visit.
+struct FwdItem {
+  int bh, q0, bkv;
+  int kb[2], ke[2];  // key-tile range of tile A and tile B
+  int ub, ue;        // their union, loaded once
+};
+
+// The n-th item of this CTA, or false past its last.  Items are numbered
+// heaviest causal rows first (the pair index slowest); round n of the grid
+// takes items [n * G, n * G + G), CTA c the c-th of them in even rounds and
+// the (G - 1 - c)-th in odd ones, so each CTA's heavy and light items pair up.
+template <bool CAUSAL, bool WINDOW>
+__device__ __forceinline__ bool fwd_item(const FwdParams& p, int n, FwdItem* it) {
+  const long long G = gridDim.x, c = blockIdx.x;
+  const long long k = n * G + ((n & 1) ? G - 1 - c : c);
+  if (k >= p.n_items) return false;
+  const int y = (int)(k / p.n_bh);
+  it->bh = (int)(k - (long long)y * p.n_bh);
+  const int b = it->bh / p.Hq, h = it->bh - b * p.Hq;
+  it->q0 = (p.n_pairs - 1 - y) * (2 * BM);
+  it->bkv = b * p.Hkv + h / p.G;
+  kv_range_for<CAUSAL, WINDOW>(p, it->q0, &it->kb[0], &it->ke[0]);
+  kv_range_for<CAUSAL, WINDOW>(p, it->q0 + BM, &it->kb[1], &it->ke[1]);
+  // Tile B's rows follow tile A's, so B's range starts and ends no earlier
+  // than A's, and starts no later than A's end: the union has no gap and
+  // every key tile in it is needed by A or B.
+  it->ub = it->ke[0] > it->kb[0] ? it->kb[0] : it->kb[1];
+  it->ue = max(it->ke[0], it->ke[1]);
+  return true;
+}
+
 // WINDOW (causal only): the sliding-window terms are compiled in only where
 // a window is set, so the plain causal and full masks keep their lean code.
 template <int HD, int HDV, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<HD, HDV>;
   constexpr int NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars;
+  uint64_t* q_full = bars;           // [2] per tile
+  uint64_t* q_empty = q_full + 2;    // [2]
   // One "full" barrier per ring slot covers both K_j and V_j, so the MMA
   // thread checks a key tile once; K and V are released separately (K after
   // the last S that reads it, V after the last P.V), so K_{j+NS} can load
   // before V_j's readers are done.
-  uint64_t* kv_full = q_full + 1;
+  uint64_t* kv_full = q_empty + 2;
   uint64_t* k_empty = kv_full + NS;
   uint64_t* v_empty = k_empty + NS;
   uint64_t* s_full = v_empty + NS;  // [2] per tile
@@ -138,63 +181,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int b = bh / p.Hq, h = bh - b * p.Hq;
-  const int q0 = (gridDim.y - 1 - blockIdx.y) * (2 * BM);  // longest causal rows first
-  const int bkv = b * p.Hkv + h / p.G;
-  int kb[2], ke[2];  // key-tile range of tile A and tile B
-  kv_range_for<CAUSAL, WINDOW>(p, q0, &kb[0], &ke[0]);
-  kv_range_for<CAUSAL, WINDOW>(p, q0 + BM, &kb[1], &ke[1]);
-  // Union of the two ranges, loaded once.  Tile B's rows follow tile A's, so
-  // B's range starts and ends no earlier than A's, and starts no later than
-  // A's end: the union has no gap and every key tile in it is needed by A or B.
-  const int ub = ke[0] > kb[0] ? kb[0] : kb[1];
-  const int ue = max(ke[0], ke[1]);
-  const int nkv_max = ue - ub;  // key tiles the CTA loads
-  const bool has_b = q0 + BM < p.Tq;
+  const uint32_t q_buf = smem_u32(smem + C::OFF_Q);
+  const uint32_t k_base = smem_u32(smem + C::OFF_K);
+  const uint32_t v_base = smem_u32(smem + C::OFF_V);
+  bool withhold_q = false;
+#ifdef FA_TEST_HOOKS
+  withhold_q = p.test_withhold_q != 0;
+#endif
+
+  // Producer state; the first item's Q and its first NS key/value tiles (the
+  // ring slots are all free) are issued during set-up, before TMEM allocation
+  // and the CTA-wide barrier, so their memory latency overlaps the set-up.
+  int nq[2] = {0, 0};  // Q_X loads issued (the producer) / waited for (the MMA thread)
+  int pre_kv = 0;      // key/value tiles of item 0 issued during set-up
+  auto load_q = [&](const FwdItem& it, int x) {
+    if (!withhold_q) {
+      mbar_arrive_expect_tx(&q_full[x], C::Q_BYTES);
+#pragma unroll
+      for (int cb = 0; cb < HD / 64; ++cb)
+        tma_load_3d(smem + C::OFF_Q + x * C::Q_BYTES + cb * BM * 128, &tmQ, &q_full[x], cb * 64, it.q0 + x * BM,
+                    it.bh);
+    }
+    ++nq[x];
+  };
+  auto load_k = [&](const FwdItem& it, int jj, int s) {
+    mbar_arrive_expect_tx(&kv_full[s], C::K_BYTES + C::V_BYTES);
+#pragma unroll
+    for (int cb = 0; cb < HD / 64; ++cb)
+      tma_load_3d(smem + C::OFF_K + s * C::K_BYTES + cb * BN * 128, &tmK, &kv_full[s], cb * 64,
+                  (it.ub + jj) * BN, it.bkv);
+  };
+  auto load_v = [&](const FwdItem& it, int jj, int s) {
+#pragma unroll
+    for (int cb = 0; cb < HDV / 64; ++cb)
+      tma_load_3d(smem + C::OFF_V + s * C::V_BYTES + cb * BN * 128, &tmV, &kv_full[s], cb * 64,
+                  (it.ub + jj) * BN, it.bkv);
+  };
 
   if (threadIdx.x == 0) {
     *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;  // swizzled tiles need 1024 B alignment
-    mbar_init(q_full, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&q_full[x], 1);
+      mbar_init(&q_empty[x], 1);
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 128);
+      mbar_init(&o_done[x], 1);
+    }
     for (int s = 0; s < NS; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 128);
-      mbar_init(&o_done[x], 1);
-    }
     mbar_init(drain, 1);
     fence_mbar_init();
-    // The first loads (Q_A, Q_B and the first NS key/value tiles, whose ring
-    // slots are free) are issued here, before TMEM allocation and the CTA-wide
-    // barrier, so their memory latency overlaps the set-up.
-    if (*abort_flag == 0 && nkv_max > 0) {
+    FwdItem it;
+    if (*abort_flag == 0 && fwd_item<CAUSAL, WINDOW>(p, 0, &it)) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-#ifdef FA_TEST_HOOKS
-      if (!p.test_withhold_q)
-#endif
-      {
-        mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::Q_BYTES);
 #pragma unroll
-        for (int cb = 0; cb < HD / 64; ++cb) {
-          tma_load_3d(smem + C::OFF_Q + cb * BM * 128, &tmQ, q_full, cb * 64, q0, bh);
-          if (has_b) tma_load_3d(smem + C::OFF_Q + C::Q_BYTES + cb * BM * 128, &tmQ, q_full, cb * 64, q0 + BM, bh);
-        }
-      }
-      for (int jj = 0; jj < NS && jj < nkv_max; ++jj) {
-        const int kv0 = (ub + jj) * BN;
-        mbar_arrive_expect_tx(&kv_full[jj], C::K_BYTES + C::V_BYTES);
-#pragma unroll
-        for (int cb = 0; cb < HD / 64; ++cb)
-          tma_load_3d(smem + C::OFF_K + jj * C::K_BYTES + cb * BN * 128, &tmK, &kv_full[jj], cb * 64, kv0, bkv);
-#pragma unroll
-        for (int cb = 0; cb < HDV / 64; ++cb)
-          tma_load_3d(smem + C::OFF_V + jj * C::V_BYTES + cb * BN * 128, &tmV, &kv_full[jj], cb * 64, kv0, bkv);
+      for (int x = 0; x < 2; ++x)
+        if (it.ke[x] > it.kb[x]) load_q(it, x);
+      for (; pre_kv < NS && pre_kv < it.ue - it.ub; ++pre_kv) {
+        load_k(it, pre_kv, pre_kv);
+        load_v(it, pre_kv, pre_kv);
       }
     }
   }
@@ -206,38 +256,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const bool run = (*abort_flag == 0) && nkv_max > 0;
+  const bool run = *abort_flag == 0;
 
   if (warp < 4) {
     setmaxnreg_dec<kRegsLow>();
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       if (lane == 0 && run) {
-        // Q and the first NS key/value tiles were issued during set-up.
-        int kv_last[NS];  // last ring pass whose K and V loads were both issued, per slot
+        int g = pre_kv;     // ring position of the next key/value tile (running over items)
+        int kv_last[NS];    // last ring pass whose K and V loads were both issued, per slot
         bool half = false;  // a K load was issued whose V load was not (abort in between)
 #pragma unroll
-        for (int s = 0; s < NS; ++s) kv_last[s] = s < nkv_max ? 0 : -1;
-        for (int jj = NS; jj < nkv_max; ++jj) {  // ring position jj holds key tile ub + jj
-          const int s = jj % NS, u = jj / NS, kv0 = (ub + jj) * BN;
-          if (!mbar_wait(&k_empty[s], (u & 1) ^ 1, abort_flag)) break;
-          mbar_arrive_expect_tx(&kv_full[s], C::K_BYTES + C::V_BYTES);
+        for (int s = 0; s < NS; ++s) kv_last[s] = s < pre_kv ? 0 : -1;
+        bool ok = true;
+        FwdItem it;
+        for (int n = 0; ok && fwd_item<CAUSAL, WINDOW>(p, n, &it); ++n) {
+          if (n > 0) {
 #pragma unroll
-          for (int cb = 0; cb < HD / 64; ++cb)
-            tma_load_3d(smem + C::OFF_K + s * C::K_BYTES + cb * BN * 128, &tmK, &kv_full[s], cb * 64, kv0, bkv);
-          half = true;
-          if (!mbar_wait(&v_empty[s], (u & 1) ^ 1, abort_flag)) break;
-#pragma unroll
-          for (int cb = 0; cb < HDV / 64; ++cb)
-            tma_load_3d(smem + C::OFF_V + s * C::V_BYTES + cb * BN * 128, &tmV, &kv_full[s], cb * 64, kv0, bkv);
-          half = false;
-          kv_last[s] = u;
+            for (int x = 0; x < 2; ++x) {
+              if (it.ke[x] <= it.kb[x]) continue;
+              // Q_X's buffer is free once the previous item's last S_X has read it.
+              if (nq[x] > 0 && !mbar_wait(&q_empty[x], (nq[x] - 1) & 1, abort_flag)) { ok = false; break; }
+              load_q(it, x);
+            }
+          }
+          for (int jj = n == 0 ? pre_kv : 0; ok && jj < it.ue - it.ub; ++jj, ++g) {
+            const int s = g % NS, u = g / NS;
+            if (!mbar_wait(&k_empty[s], (u & 1) ^ 1, abort_flag)) { ok = false; break; }
+            load_k(it, jj, s);
+            half = true;
+            if (!mbar_wait(&v_empty[s], (u & 1) ^ 1, abort_flag)) { ok = false; break; }
+            load_v(it, jj, s);
+            half = false;
+            kv_last[s] = u;
+          }
         }
         // Every issued copy must land before the CTA releases its shared memory.
-#ifdef FA_TEST_HOOKS
-        if (!p.test_withhold_q)
-#endif
-          mbar_wait_bounded(q_full, 0);
+        if (!withhold_q)
+#pragma unroll
+          for (int x = 0; x < 2; ++x)
+            if (nq[x] > 0) mbar_wait_bounded(&q_full[x], (nq[x] - 1) & 1);
 #pragma unroll
         for (int s = 0; s < NS; ++s)
           if (kv_last[s] >= 0) mbar_wait_bounded(&kv_full[s], kv_last[s] & 1);
@@ -254,60 +312,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && run) {
         constexpr uint32_t idS = idesc_bf16(BM, BN, 0, 0);
         constexpr uint32_t idPV = idesc_bf16(BM, HDV, 0, 1);
-        const uint32_t k_base = smem_u32(smem + C::OFF_K);
-        const uint32_t v_base = smem_u32(smem + C::OFF_V);
-        bool ok = mbar_wait(q_full, 0, abort_flag);
-        if (ok) tc_fence_after();
-        auto active = [&](int x, int j) { return j >= kb[x] && j < ke[x]; };
-        // S_X(j) = Q_X K_j^T into TMEM [128 X, 128 X + 128)
-        // Tile B's groups use the K_j / V_j tile A's groups have just waited
-        // for; re-waiting would only leave the tensor pipe idle for the round trip.
-        auto issue_s = [&](int x, int j) -> bool {
-          const int s = (j - ub) % NS;
-          if (!(x == 1 && active(0, j)) && !mbar_wait(&kv_full[s], ((j - ub) / NS) & 1, abort_flag)) return false;
-          tc_fence_after();
-          const uint32_t q_base = smem_u32(smem + C::OFF_Q + x * C::Q_BYTES);
-#pragma unroll
-          for (int k = 0; k < HD / 16; ++k) {
-            const uint64_t a = desc_kmajor(q_base + (k >> 2) * (BM * 128) + (k & 3) * 32);
-            const uint64_t bd = desc_kmajor(k_base + s * C::K_BYTES + (k >> 2) * (BN * 128) + (k & 3) * 32);
-            mma_ss(tmem + x * 128, a, bd, idS, k > 0 ? 1u : 0u);
-          }
-          mma_commit(&s_full[x]);
-          return true;
-        };
-        // O_X += P_X(j) V_j with P_X read from TMEM (packed bf16 over S_X)
-        auto issue_pv = [&](int x, int j) -> bool {
-          const int s = (j - ub) % NS;
-          // V_j landed with K_j: the S(j) MMA before this P.V waited for both.
-          if (!mbar_wait(&p_full[x], (j - kb[x]) & 1, abort_flag)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < BN / 16; ++k) {
-            const uint64_t bd = desc_mnmajor(v_base + s * C::V_BYTES + k * 2048, BN * 128);
-            mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, bd, idPV, (j > kb[x] || k > 0) ? 1u : 0u);
-          }
-          return true;
-        };
-        // A tile whose range starts at ub gets its first S up front; tile B, if
-        // it starts later, gets it in the loop below one step before its range.
-        if (ok && active(0, ub)) ok = issue_s(0, ub);
-        if (ok && active(1, ub)) ok = issue_s(1, ub);
-        if (ok) mma_commit(&k_empty[0]);
-        for (int j = ub; ok && j < ue; ++j) {
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (active(x, j)) {
-              if (!issue_pv(x, j)) { ok = false; break; }
-              if (x == 1 || !active(1, j)) mma_commit(&v_empty[(j - ub) % NS]);  // last reader of V_j
+        int np[2] = {0, 0};  // p_full phases waited for, per tile
+        int base = 0;        // ring position of the current item's first key tile
+        bool ok = true;
+        FwdItem it;
+        for (int n = 0; ok && fwd_item<CAUSAL, WINDOW>(p, n, &it); ++n) {
+          auto active = [&](int x, int j) { return j >= it.kb[x] && j < it.ke[x]; };
+          // S_X(j) = Q_X K_j^T into TMEM [128 X, 128 X + 128)
+          // Tile B's groups use the K_j / V_j tile A's groups have just waited
+          // for; re-waiting would only leave the tensor pipe idle for the round trip.
+          auto issue_s = [&](int x, int j) -> bool {
+            const int pos = base + (j - it.ub), s = pos % NS;
+            if (j == it.kb[x]) {  // the tile's first S of this item: wait for its Q
+              if (!mbar_wait(&q_full[x], nq[x] & 1, abort_flag)) return false;
+              ++nq[x];
             }
-            if (active(x, j + 1)) {
-              if (!issue_s(x, j + 1)) { ok = false; break; }
-              if (x == 1 || !active(1, j + 1)) mma_commit(&k_empty[(j + 1 - ub) % NS]);  // last reader of K_{j+1}
-            } else if (active(x, j)) {
-              mma_commit(&o_done[x]);
+            if (!(x == 1 && active(0, j)) && !mbar_wait(&kv_full[s], (pos / NS) & 1, abort_flag)) return false;
+            tc_fence_after();
+            const uint32_t q_base = q_buf + x * C::Q_BYTES;
+#pragma unroll
+            for (int k = 0; k < HD / 16; ++k) {
+              const uint64_t a = desc_kmajor(q_base + (k >> 2) * (BM * 128) + (k & 3) * 32);
+              const uint64_t bd = desc_kmajor(k_base + s * C::K_BYTES + (k >> 2) * (BN * 128) + (k & 3) * 32);
+              mma_ss(tmem + x * 128, a, bd, idS, k > 0 ? 1u : 0u);
+            }
+            mma_commit(&s_full[x]);
+            if (j == it.ke[x] - 1) mma_commit(&q_empty[x]);  // last reader of Q_X in this item
+            return true;
+          };
+          // O_X += P_X(j) V_j with P_X read from TMEM (packed bf16 over S_X)
+          auto issue_pv = [&](int x, int j) -> bool {
+            const int s = (base + j - it.ub) % NS;
+            // V_j landed with K_j: the S(j) MMA before this P.V waited for both.
+            if (!mbar_wait(&p_full[x], np[x] & 1, abort_flag)) return false;
+            ++np[x];
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < BN / 16; ++k) {
+              const uint64_t bd = desc_mnmajor(v_base + s * C::V_BYTES + k * 2048, BN * 128);
+              mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, bd, idPV, (j > it.kb[x] || k > 0) ? 1u : 0u);
+            }
+            return true;
+          };
+          if (it.ue > it.ub) {
+            // A tile whose range starts at ub gets its first S up front; tile B,
+            // if it starts later, gets it in the loop below one step before its range.
+            if (ok && active(0, it.ub)) ok = issue_s(0, it.ub);
+            if (ok && active(1, it.ub)) ok = issue_s(1, it.ub);
+            if (ok) mma_commit(&k_empty[base % NS]);
+          }
+          for (int j = it.ub; ok && j < it.ue; ++j) {
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              if (active(x, j)) {
+                if (!issue_pv(x, j)) { ok = false; break; }
+                if (x == 1 || !active(1, j)) mma_commit(&v_empty[(base + j - it.ub) % NS]);  // last reader of V_j
+              }
+              if (active(x, j + 1)) {
+                if (!issue_s(x, j + 1)) { ok = false; break; }
+                if (x == 1 || !active(1, j + 1))
+                  mma_commit(&k_empty[(base + j + 1 - it.ub) % NS]);  // last reader of K_{j+1}
+              } else if (active(x, j)) {
+                mma_commit(&o_done[x]);
+              }
             }
           }
+          base += it.ue - it.ub;
         }
         // Let every MMA issued above finish before TMEM is released.
         mma_commit(drain);
@@ -318,110 +388,113 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax + epilogue of tile x
     setmaxnreg_inc<kRegsHigh>();
     const int x = (warp - 4) >> 2;
-    const int kbx = x ? kb[1] : kb[0];  // first key tile of this tile's range
-    const int nkv = (x ? ke[1] : ke[0]) - kbx;
-    const int qx0 = q0 + x * BM;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // row inside the tile == TMEM lane
-    const int i = qx0 + r;           // query row
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + x * 128 + lane_base;
     const uint32_t tO = tmem + 256 + x * 128 + lane_base;
     const float sl2 = p.scale_log2;
     const float NEG_INF = -__int_as_float(0x7f800000);
-    float m_ref = NEG_INF;  // reference max (log2 units) the P values are taken against
-    float l = 0.f;
+    int ns = 0, no = 0;  // s_full / o_done phases waited for
     bool ok = run;
-    for (int jx = 0; ok && jx < nkv; ++jx) {  // jx-th key tile of this tile's range
-      // the warp agrees on the outcome before its collective TMEM loads
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[x], jx & 1, abort_flag))) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sr[BN];
+    FwdItem it;
+    for (int n = 0; ok && fwd_item<CAUSAL, WINDOW>(p, n, &it); ++n) {
+      const int kbx = x ? it.kb[1] : it.kb[0];  // first key tile of this tile's range
+      const int nkv = (x ? it.ke[1] : it.ke[0]) - kbx;
+      const int qx0 = it.q0 + x * BM;
+      const int i = qx0 + r;  // query row
+      float m_ref = NEG_INF;  // reference max (log2 units) the P values are taken against
+      float l = 0.f;
+      for (int jx = 0; ok && jx < nkv; ++jx) {  // jx-th key tile of this tile's range
+        // the warp agrees on the outcome before its collective TMEM loads
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[x], ns & 1, abort_flag))) { ok = false; break; }
+        ++ns;
+        tc_fence_after();
+        uint32_t sr[BN];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-      tmem_wait_ld();
-      const int kv0 = (kbx + jx) * BN;
-      // window: the tile's last row starts its window past this key tile's start
-      const bool win_mask = WINDOW && qx0 + BM - 1 + p.causal_off - p.window + 1 > kv0;
-      const bool need_mask = (kv0 + BN > p.Tk) || (CAUSAL && kv0 + BN - 1 > qx0 + p.causal_off) || win_mask;
-      if (need_mask) {
-        int lim = p.Tk - kv0;  // columns [lo, lim) are visible to row i
-        if (CAUSAL) lim = min(lim, i + p.causal_off + 1 - kv0);
-        const int lo = win_mask ? i + p.causal_off - p.window + 1 - kv0 : -BN;
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        tmem_wait_ld();
+        const int kv0 = (kbx + jx) * BN;
+        // window: the tile's last row starts its window past this key tile's start
+        const bool win_mask = WINDOW && qx0 + BM - 1 + p.causal_off - p.window + 1 > kv0;
+        const bool need_mask = (kv0 + BN > p.Tk) || (CAUSAL && kv0 + BN - 1 > qx0 + p.causal_off) || win_mask;
+        if (need_mask) {
+          int lim = p.Tk - kv0;  // columns [lo, lim) are visible to row i
+          if (CAUSAL) lim = min(lim, i + p.causal_off + 1 - kv0);
+          const int lo = win_mask ? i + p.causal_off - p.window + 1 - kv0 : -BN;
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c >= lim || c < lo) sr[c] = __float_as_uint(NEG_INF);
-      }
-      // row max: eight independent three-input max chains (short dependency depth)
-      float pm[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) pm[k] = __uint_as_float(sr[k]);
-#pragma unroll
-      for (int c = 8; c < BN; c += 16)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) pm[k] = fmax3(pm[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
-      const float mt = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
-      const float mt2 = mt * sl2;
-      float m_new = m_ref;
-      if (mt2 > m_ref + kRescaleThreshold) m_new = mt2;  // also taken when m_ref == -inf
-      // Does this row's O need rescaling, and does any row of the warp's?  (The
-      // vote is taken here, where fewer registers are live than after exp2.)
-      const bool rescale = jx > 0 && m_new != m_ref && m_ref != NEG_INF;
-      const bool warp_rescale = __any_sync(0xffffffffu, rescale);
-      const float base = (m_new == NEG_INF) ? 0.f : m_new;
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), nbase2 = f2_pack(-base, -base);
-      // exponentials (argument and row sum on packed pairs); P (packed bf16)
-      // goes over the already-loaded scores in TMEM 16 columns at a time
-      uint64_t rs[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[32 * c + 2 * e]), __uint_as_float(sr[32 * c + 2 * e + 1])),
-                                    sl2x2, nbase2);
-          const float e0 = ex2(f2_lo(x)), e1 = ex2(f2_hi(x));
-          rs[e & 3] = f2_add(rs[e & 3], f2_pack(e0, e1));
-          pk[e] = pack_bf16x2(e0, e1);
+          for (int c = 0; c < BN; ++c)
+            if (c >= lim || c < lo) sr[c] = __float_as_uint(NEG_INF);
         }
-        tmem_st16(tS + 16 * c, pk);
-      }
-      const uint64_t rs2 = f2_add(f2_add(rs[0], rs[1]), f2_add(rs[2], rs[3]));
-      const float rowsum = f2_lo(rs2) + f2_hi(rs2);
-      // O_X is idle here: the P.V of tile j-1 completed before S_X(j) did.
-      const float alpha = (m_new == m_ref) ? 1.f : (m_ref == NEG_INF ? 0.f : ex2(m_ref - m_new));
-      l = l * alpha + rowsum;
-      // TMEM loads and stores are warp-collective: when any row of the warp
-      // must rescale its O row, every lane takes part (factor 1 where not).
-      if (warp_rescale) {
-        const float a = rescale ? alpha : 1.f;
+        // row max: eight independent three-input max chains (short dependency depth)
+        float pm[8];
 #pragma unroll
-        for (int c = 0; c < HDV / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_wait_ld();
+        for (int k = 0; k < 8; ++k) pm[k] = __uint_as_float(sr[k]);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
-          tmem_st32(tO + c * 32, o);
+        for (int c = 8; c < BN; c += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) pm[k] = fmax3(pm[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+        const float mt = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+        const float mt2 = mt * sl2;
+        float m_new = m_ref;
+        if (mt2 > m_ref + kRescaleThreshold) m_new = mt2;  // also taken when m_ref == -inf
+        // Does this row's O need rescaling, and does any row of the warp's?  (The
+        // vote is taken here, where fewer registers are live than after exp2.)
+        const bool rescale = jx > 0 && m_new != m_ref && m_ref != NEG_INF;
+        const bool warp_rescale = __any_sync(0xffffffffu, rescale);
+        const float base = (m_new == NEG_INF) ? 0.f : m_new;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nbase2 = f2_pack(-base, -base);
+        // exponentials (argument and row sum on packed pairs); P (packed bf16)
+        // goes over the already-loaded scores in TMEM 16 columns at a time
+        uint64_t rs[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const uint64_t xv = f2_fma(
+                f2_pack(__uint_as_float(sr[32 * c + 2 * e]), __uint_as_float(sr[32 * c + 2 * e + 1])), sl2x2, nbase2);
+            const float e0 = ex2(f2_lo(xv)), e1 = ex2(f2_hi(xv));
+            rs[e & 3] = f2_add(rs[e & 3], f2_pack(e0, e1));
+            pk[e] = pack_bf16x2(e0, e1);
+          }
+          tmem_st16(tS + 16 * c, pk);
         }
+        const uint64_t rs2 = f2_add(f2_add(rs[0], rs[1]), f2_add(rs[2], rs[3]));
+        const float rowsum = f2_lo(rs2) + f2_hi(rs2);
+        // O_X is idle here: the P.V of tile j-1 completed before S_X(j) did.
+        const float alpha = (m_new == m_ref) ? 1.f : (m_ref == NEG_INF ? 0.f : ex2(m_ref - m_new));
+        l = l * alpha + rowsum;
+        // TMEM loads and stores are warp-collective: when any row of the warp
+        // must rescale its O row, every lane takes part (factor 1 where not).
+        if (warp_rescale) {
+          const float a = rescale ? alpha : 1.f;
+#pragma unroll
+          for (int c = 0; c < HDV / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+            tmem_st32(tO + c * 32, o);
+          }
+        }
+        m_ref = m_new;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[x]);
       }
-      m_ref = m_new;
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&p_full[x]);
-    }
-    // ---- epilogue: O / l -> bf16 -> shared (this tile's Q buffer, free now) -> TMA store; L -> global
-    if (ok && nkv > 0) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&o_done[x], 0, abort_flag))) ok = false;
-      tc_fence_after();
-    }
-    // All 128 threads of the warpgroup agree on whether to write (a timeout
-    // anywhere in the CTA cancels the epilogue), so its barriers never split.
-    const bool mine = ((nkv == 0) || ok) && *abort_flag == 0 && qx0 < p.Tq;
-    if (named_bar_and(1 + x, 128, mine)) {
+      // ---- epilogue: O / l -> bf16 -> global (one row per thread); L -> global
+      if (ok && nkv > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[x], no & 1, abort_flag))) ok = false;
+        ++no;
+        tc_fence_after();
+      }
+      if (!ok || qx0 >= p.Tq) continue;  // (a tile past the last row has nothing to write)
+      const bool row_ok = i < p.Tq;
+      if (row_ok) p.L[(size_t)it.bh * p.Tq + i] = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : NEG_INF;
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      if (i < p.Tq) p.L[(size_t)bh * p.Tq + i] = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : NEG_INF;
-      uint8_t* Os = smem + C::OFF_O + x * C::O_STRIDE;
+      uint4* orow = reinterpret_cast<uint4*>(p.O + ((size_t)it.bh * p.Tq + (row_ok ? i : 0)) * HDV);
 #pragma unroll
       for (int c = 0; c < HDV / 32; ++c) {
         uint32_t o[32];
@@ -432,23 +505,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0u;
         }
+        if (row_ok) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t w0 = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
-          const uint32_t w1 = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
-          const uint32_t w2 = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
-          const uint32_t w3 = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
-          st_shared_v4(smem_u32(Os + (c >> 1) * (BM * 128) + sw128_offset(r, (c & 1) * 4 + q)), w0, w1, w2, w3);
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+            orow[c * 4 + q] = w;
+          }
         }
-      }
-      fence_async_smem();
-      named_bar_sync(3 + x, 128);
-      if (quad == 0 && lane == 0) {
-        prefetch_tmap(&tmO);
-#pragma unroll
-        for (int cb = 0; cb < HDV / 64; ++cb) tma_store_3d(&tmO, Os + cb * BM * 128, cb * 64, qx0, bh);
-        bulk_commit();
-        bulk_wait0();
       }
     }
   }
@@ -461,9 +528,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_flag) atomicExch(p.status, DEV_TIMEOUT);
 }
 
+// SM count of the current device (the persistent grid's size); 0 if unknown.
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess)
+    return 0;
+  return sms;
+}
+
 template <int HD, int HDV, bool CAUSAL, bool WINDOW>
 cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const CUtensorMap& mo, float* L, cudaStream_t stream) {
+                         void* O, float* L, cudaStream_t stream) {
   using C = FwdCfg<HD, HDV>;
   const void* fn = reinterpret_cast<const void*>(fa_fwd_kernel<HD, HDV, CAUSAL, WINDOW>);
   cudaError_t e = fa::allow_dynamic_smem(fn, C::SMEM);
@@ -475,7 +551,10 @@ cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUt
   e = cudaFuncGetAttributes(&fa_attr, fn);
   if (e != cudaSuccess) return e;
   if (fa_attr.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
   FwdParams p;
+  p.O = static_cast<uint16_t*>(O);
   p.L = L;
   p.status = fa::device_status_word();
   p.Hq = pr.Hq;
@@ -486,19 +565,22 @@ cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUt
   p.causal_off = pr.Tk - pr.Tq;
   p.window = pr.causal ? pr.window : 0;
   p.kv_tiles = pr.kv_tiles();
+  p.n_bh = pr.B * pr.Hq;
+  p.n_pairs = (pr.q_tiles() + 1) / 2;
+  p.n_items = (long long)p.n_bh * p.n_pairs;
   p.scale_log2 = pr.scale * 1.4426950408889634f;
   p.test_withhold_q = fa::test_withhold() == fa::kWithholdFwdQ;
-  dim3 grid(pr.B * pr.Hq, (pr.q_tiles() + 1) / 2);
-  fa_fwd_kernel<HD, HDV, CAUSAL, WINDOW><<<grid, kThreads, C::SMEM, stream>>>(mq, mk, mv, mo, p);
+  const int grid = (int)(p.n_items < sms ? p.n_items : sms);
+  fa_fwd_kernel<HD, HDV, CAUSAL, WINDOW><<<grid, kThreads, C::SMEM, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
 template <int HD, int HDV>
 cudaError_t launch_fwd_dims(const fa::Problem& pr, const CUtensorMap& mq, const CUtensorMap& mk,
-                            const CUtensorMap& mv, const CUtensorMap& mo, float* L, cudaStream_t stream) {
-  if (!pr.causal) return launch_fwd_t<HD, HDV, false, false>(pr, mq, mk, mv, mo, L, stream);
-  if (pr.window) return launch_fwd_t<HD, HDV, true, true>(pr, mq, mk, mv, mo, L, stream);
-  return launch_fwd_t<HD, HDV, true, false>(pr, mq, mk, mv, mo, L, stream);
+                            const CUtensorMap& mv, void* O, float* L, cudaStream_t stream) {
+  if (!pr.causal) return launch_fwd_t<HD, HDV, false, false>(pr, mq, mk, mv, O, L, stream);
+  if (pr.window) return launch_fwd_t<HD, HDV, true, true>(pr, mq, mk, mv, O, L, stream);
+  return launch_fwd_t<HD, HDV, true, false>(pr, mq, mk, mv, O, L, stream);
 }
 
 __global__ void fa_fwd_empty_keys(uint32_t* O_words, size_t n_words, float* L, size_t n_rows) {
@@ -524,19 +606,18 @@ cudaError_t launch_forward(const Problem& pr, const void* Q, const void* K, cons
     ++*launches;
     return cudaGetLastError();
   }
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv;
   if (!encode_rows_bf16(&mq, Q, pr.d, pr.Tq, (long long)pr.B * pr.Hq) ||
       !encode_rows_bf16(&mk, K, pr.d, pr.Tk, (long long)pr.B * pr.Hkv) ||
-      !encode_rows_bf16(&mv, V, pr.dv, pr.Tk, (long long)pr.B * pr.Hkv) ||
-      !encode_rows_bf16(&mo, O, pr.dv, pr.Tq, (long long)pr.B * pr.Hq))
+      !encode_rows_bf16(&mv, V, pr.dv, pr.Tk, (long long)pr.B * pr.Hkv))
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (pr.d == 64)
-    e = pr.dv == 64 ? launch_fwd_dims<64, 64>(pr, mq, mk, mv, mo, L, stream)
-                    : launch_fwd_dims<64, 128>(pr, mq, mk, mv, mo, L, stream);
+    e = pr.dv == 64 ? launch_fwd_dims<64, 64>(pr, mq, mk, mv, O, L, stream)
+                    : launch_fwd_dims<64, 128>(pr, mq, mk, mv, O, L, stream);
   else
-    e = pr.dv == 64 ? launch_fwd_dims<128, 64>(pr, mq, mk, mv, mo, L, stream)
-                    : launch_fwd_dims<128, 128>(pr, mq, mk, mv, mo, L, stream);
+    e = pr.dv == 64 ? launch_fwd_dims<128, 64>(pr, mq, mk, mv, O, L, stream)
+                    : launch_fwd_dims<128, 128>(pr, mq, mk, mv, O, L, stream);
   if (e == cudaSuccess) ++*launches;
   return e;
 }
