@@ -15,6 +15,12 @@ key tile), O_X per warp = (item, last key tile accumulated). A run fails on a
 deadlock, an arrival for a phase the barrier is not collecting, a parity wait
 that finds its barrier two phases ahead, or a read of the wrong version.
 
+The issuing thread checks K_j / V_j only where nothing else vouches for
+them: tile B's S uses the key tile tile A has just waited for, and with a
+4-deep K/V ring (NS >= 3, as in the kernel) the softmax of tile X checks the
+next key tile's K / V before it arrives on P_X's barrier, so inside an item
+the issuer's wait for P_X(j-1) also covers S_X(j).
+
 Item sequences are random but keep the kernel's invariants: tile B's range
 starts and ends no earlier than A's and starts no later than A's end; either
 range may be empty. Planted protocol mistakes must each be caught, so the
@@ -50,8 +56,9 @@ def random_items(rnd, n_items):
     return items
 
 
-def run(items, NS, seed, mutation=None):
+def run(items, NS, seed, mutation=None, copy_prob=1.0):
     rnd = random.Random(seed)
+    kv_soft = NS >= 3
     cnt = {"drain": 1}
     for x in (0, 1):
         cnt.update({f"q_full{x}": 1, f"q_empty{x}": 1, f"s_full{x}": 1, f"p_full{x}": 128, f"o_done{x}": 1})
@@ -133,13 +140,13 @@ def run(items, NS, seed, mutation=None):
         for n, it in enumerate(items):
             ub, ue = union(it)
 
-            def issue_s(x, j):
+            def issue_s(x, j, wait_kv):
                 pos = base + j - ub
                 s = pos % NS
                 if j == it[x][0]:
                     yield ("wait", f"q_full{x}", nq[x])
                     nq[x] += 1
-                if not (x == 1 and active(it, 0, j)):
+                if wait_kv:
                     yield ("wait", f"kv_full{s}", pos // NS)
                 pipe_q.append(("S", n, x, j, s))
                 pipe_q.append(("commit", f"s_full{x}"))
@@ -156,7 +163,7 @@ def run(items, NS, seed, mutation=None):
             if ue > ub:
                 for x in (0, 1):
                     if active(it, x, ub):
-                        yield from issue_s(x, ub)
+                        yield from issue_s(x, ub, not (x == 1 and active(it, 0, ub)))
                 pipe_q.append(("commit", f"k_empty{base % NS}"))
             for j in range(ub, ue):
                 for x in (0, 1):
@@ -168,7 +175,11 @@ def run(items, NS, seed, mutation=None):
                         if x == 1 or not active(it, 1, j):
                             pipe_q.append(("commit", f"v_empty{(base + j - ub) % NS}"))
                     if active(it, x, j + 1):
-                        yield from issue_s(x, j + 1)
+                        covered = ((x == 1 and active(it, 0, j + 1) and (not kv_soft or active(it, 0, j)))
+                                   or (kv_soft and active(it, x, j)))
+                        if mutation == "issuer-trusts-uncovered-kv":
+                            covered = True
+                        yield from issue_s(x, j + 1, not covered)
                         if x == 1 or not active(it, 1, j + 1):
                             pipe_q.append(("commit", f"k_empty{(base + j + 1 - ub) % NS}"))
                     elif last_pv and mutation != "o_done-before-last-PV":
@@ -196,8 +207,12 @@ def run(items, NS, seed, mutation=None):
 
     def softmax(x, w):
         ns = no = 0
+        base = 0
         deferred = None  # mutation "epilogue-after-next-P": the O read put off past the next P
         for n, it in enumerate(items):
+            ub, ue = union(it)
+            item_base = base
+            base += ue - ub
             kb, ke = it[x]
             for j in range(kb, ke):
                 yield ("wait", f"s_full{x}", ns)
@@ -207,6 +222,9 @@ def run(items, NS, seed, mutation=None):
                 yield None
                 if j > kb:  # a lazy rescale of the O row (taken or not, it must be safe)
                     rd(("O", x, w), (n, j - 1))
+                if kv_soft and w == 0 and j + 1 < ke and mutation != "softmax-skips-kv-check":
+                    pos = item_base + j + 1 - ub
+                    yield ("wait", f"kv_full{pos % NS}", pos // NS)
                 arrive(f"p_full{x}", ns - 1, 32)
                 yield None
                 if deferred is not None:
@@ -238,8 +256,8 @@ def run(items, NS, seed, mutation=None):
         ready = [n for n in procs if n not in done and (pending[n] is None or can_pass(pending[n][1], pending[n][2]))]
         if pipe_q:
             ready.append("pipe")
-        if copies:
-            ready.append("copy")
+        if copies and (not ready or rnd.random() < copy_prob):
+            ready.append("copy")  # copy_prob < 1 makes loads land late
         if not ready:
             if len(done) == len(procs):
                 if comp["drain"] != 1:
@@ -278,7 +296,7 @@ def test_protocol_is_free_of_deadlock_aliasing_and_hazards(NS):
     for trial in range(120):
         items = random_items(rnd, rnd.randrange(1, 6))
         for seed in range(6):
-            run(items, NS, seed=trial * 100 + seed)
+            run(items, NS, seed=trial * 100 + seed, copy_prob=0.1 if seed % 3 == 0 else 1.0)
 
 
 def test_causal_pairs_and_full_rows():
@@ -292,21 +310,24 @@ def test_causal_pairs_and_full_rows():
                 run(items, NS, seed)
 
 
-@pytest.mark.parametrize("mutation", [
-    "q-load-skips-q_empty",     # the next item's Q would land while S of this item still reads it
-    "q_empty-after-first-S",    # Q released after its first S instead of its last
-    "epilogue-skips-o_done",    # the epilogue would read O before the last P.V
-    "o_done-before-last-PV",    # o_done committed before the last P.V is issued
-    "epilogue-after-next-P",    # the next item's first P.V would overwrite O before the epilogue reads it
+@pytest.mark.parametrize("mutation, NS", [
+    ("q-load-skips-q_empty", 2),        # the next item's Q would land while S of this item still reads it
+    ("q_empty-after-first-S", 2),       # Q released after its first S instead of its last
+    ("epilogue-skips-o_done", 2),       # the epilogue would read O before the last P.V
+    ("o_done-before-last-PV", 2),       # o_done committed before the last P.V is issued
+    ("epilogue-after-next-P", 4),       # the next item's first P.V would overwrite O before the epilogue reads it
+    ("softmax-skips-kv-check", 4),      # S(j+1) would read a K tile that has not landed
+    ("issuer-trusts-uncovered-kv", 4),  # tile B's first S inside an item, with no P barrier vouching for its K
 ])
-def test_planted_protocol_mistakes_are_caught(mutation):
+def test_planted_protocol_mistakes_are_caught(mutation, NS):
     rnd = random.Random(7)
     failures = 0
-    for trial in range(60):
-        items = random_items(rnd, rnd.randrange(2, 5))
+    # random item sequences, plus one where tile B starts exactly where tile A ends
+    lists = [random_items(rnd, rnd.randrange(2, 5)) for _ in range(60)] + [[((0, 2), (2, 4)), ((0, 1), (1, 3))] * 2] * 40
+    for trial, items in enumerate(lists):
         for seed in range(4):
             try:
-                run(items, 2, seed=trial * 10 + seed, mutation=mutation)
+                run(items, NS, seed=trial * 10 + seed, mutation=mutation, copy_prob=0.2 if seed & 1 else 1.0)
             except Err:
                 failures += 1
     assert failures > 0, f"{mutation} went unnoticed"

@@ -72,6 +72,11 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256 between
 template <int HD, int HDV>
 struct FwdCfg {
   static constexpr int NS = (HD == 64 && HDV == 64) ? 4 : 2;  // K/V ring depth
+  // With a 4-deep ring K_{j+1} / V_{j+1} have landed long before tile j's P is
+  // ready, so the softmax checks them and the MMA thread saves a barrier
+  // check per key tile.  With a 2-deep ring they often land later than that,
+  // and tying P_X(j).V to them would stall the tensor pipe.
+  static constexpr bool KV_VIA_SOFTMAX = NS >= 3;
   static constexpr int Q_BYTES = BM * HD * 2;
   static constexpr int K_BYTES = BN * HD * 2;
   static constexpr int V_BYTES = BN * HDV * 2;
@@ -318,16 +323,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         FwdItem it;
         for (int n = 0; ok && fwd_item<CAUSAL, WINDOW>(p, n, &it); ++n) {
           auto active = [&](int x, int j) { return j >= it.kb[x] && j < it.ke[x]; };
-          // S_X(j) = Q_X K_j^T into TMEM [128 X, 128 X + 128)
-          // Tile B's groups use the K_j / V_j tile A's groups have just waited
-          // for; re-waiting would only leave the tensor pipe idle for the round trip.
-          auto issue_s = [&](int x, int j) -> bool {
+          // S_X(j) = Q_X K_j^T into TMEM [128 X, 128 X + 128).  Every barrier
+          // check here costs the tensor pipe a shared-memory round trip, so
+          // K_j / V_j are checked only where nothing else vouches for them
+          // (wait_kv): tile B's S uses the key tile tile A has just waited
+          // for, and with KV_VIA_SOFTMAX, inside an item, the P_X(j-1)
+          // barrier waited for just before covers them too (the softmax
+          // checks K_j / V_j before it arrives).
+          auto issue_s = [&](int x, int j, bool wait_kv) -> bool {
             const int pos = base + (j - it.ub), s = pos % NS;
             if (j == it.kb[x]) {  // the tile's first S of this item: wait for its Q
               if (!mbar_wait(&q_full[x], nq[x] & 1, abort_flag)) return false;
               ++nq[x];
             }
-            if (!(x == 1 && active(0, j)) && !mbar_wait(&kv_full[s], (pos / NS) & 1, abort_flag)) return false;
+            if (wait_kv && !mbar_wait(&kv_full[s], (pos / NS) & 1, abort_flag)) return false;
             tc_fence_after();
             const uint32_t q_base = q_buf + x * C::Q_BYTES;
 #pragma unroll
@@ -357,8 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (it.ue > it.ub) {
             // A tile whose range starts at ub gets its first S up front; tile B,
             // if it starts later, gets it in the loop below one step before its range.
-            if (ok && active(0, it.ub)) ok = issue_s(0, it.ub);
-            if (ok && active(1, it.ub)) ok = issue_s(1, it.ub);
+            if (ok && active(0, it.ub)) ok = issue_s(0, it.ub, true);
+            if (ok && active(1, it.ub)) ok = issue_s(1, it.ub, !active(0, it.ub));
             if (ok) mma_commit(&k_empty[base % NS]);
           }
           for (int j = it.ub; ok && j < it.ue; ++j) {
@@ -369,7 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (x == 1 || !active(1, j)) mma_commit(&v_empty[(base + j - it.ub) % NS]);  // last reader of V_j
               }
               if (active(x, j + 1)) {
-                if (!issue_s(x, j + 1)) { ok = false; break; }
+                // Tile B relies on tile A's wait (or, with KV_VIA_SOFTMAX, on
+                // A's P_A(j) when A goes on to j + 1); with KV_VIA_SOFTMAX a
+                // tile's own P_X(j), just waited for, vouches for K_{j+1} / V_{j+1}.
+                const bool covered = (x == 1 && active(0, j + 1) && (!C::KV_VIA_SOFTMAX || active(0, j))) ||
+                                     (C::KV_VIA_SOFTMAX && active(x, j));
+                if (!issue_s(x, j + 1, !covered)) { ok = false; break; }
                 if (x == 1 || !active(1, j + 1))
                   mma_commit(&k_empty[(base + j + 1 - it.ub) % NS]);  // last reader of K_{j+1}
               } else if (active(x, j)) {
@@ -396,9 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     const float NEG_INF = -__int_as_float(0x7f800000);
     int ns = 0, no = 0;  // s_full / o_done phases waited for
+    int base = 0;        // ring position of the current item's first key tile
     bool ok = run;
     FwdItem it;
     for (int n = 0; ok && fwd_item<CAUSAL, WINDOW>(p, n, &it); ++n) {
+      const int item_base = base;
+      base += it.ue - it.ub;
       const int kbx = x ? it.kb[1] : it.kb[0];  // first key tile of this tile's range
       const int nkv = (x ? it.ke[1] : it.ke[0]) - kbx;
       const int qx0 = it.q0 + x * BM;
@@ -482,7 +499,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = m_new;
         tmem_wait_st();
         tc_fence_before();
+        // The MMA thread takes this barrier as word that K / V of this tile's
+        // next key tile have landed too (it issues that S right after this
+        // tile's P.V without checking them), so one thread checks them first.
+        if (C::KV_VIA_SOFTMAX && r == 0 && jx + 1 < nkv) {
+          const int pos = item_base + kbx + jx + 1 - it.ub;
+          if (!mbar_wait(&kv_full[pos % NS], (pos / NS) & 1, abort_flag)) ok = false;
+        }
         mbar_arrive(&p_full[x]);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       }
       // ---- epilogue: O / l -> bf16 -> global (one row per thread); L -> global
       if (ok && nkv > 0) {
