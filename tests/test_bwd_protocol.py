@@ -18,6 +18,9 @@ A run fails on any of these:
   pass wrongly);
 - a read that sees another version than it needs.
 
+The issuer waits for all of dS^T before dK (no half-way barrier). Loads can
+land late (the producer is held back at random).
+
 Two issue orders are checked. One is the kernel's: S^T(t+1) right after
 dV(t), with dS^T packed over the dP^T columns the elementwise warps have
 already read. The other is the kernel's earlier order, kept as a second
@@ -30,17 +33,17 @@ import random
 import pytest
 
 # Arrival counts the kernel initialises its barriers with (q_full / q_empty
-# are two-slot rings; p_ready, ds_half and ds_ready take every elementwise
-# thread, dq_empty every dQ thread).
+# are two-slot rings; p_ready and ds_ready take every elementwise thread,
+# dq_empty every dQ thread).
 CNT = dict(kv_full=1, q_full0=1, q_full1=1, q_empty0=1, q_empty1=1, do_full=1, do_empty=1, s_full=1, dp_full=1,
-           p_ready=256, ds_half=256, ds_ready=256, dq_full=1, dq_empty=128, acc_done=1)
+           p_ready=256, ds_ready=256, dq_full=1, dq_empty=128, acc_done=1)
 
 
 class Err(Exception):
     """A protocol violation found in one interleaving."""
 
 
-def run(T, own_dq, new_order, seed, mutation=None):
+def run(T, own_dq, new_order, seed, mutation=None, prod_prob=1.0):
     rnd = random.Random(seed)
     comp = {b: 0 for b in CNT}
     cur = {b: 0 for b in CNT}
@@ -113,7 +116,8 @@ def run(T, own_dq, new_order, seed, mutation=None):
         mma("S", 0); commit("s_full", 0)
         for t in range(T):
             st = t & 1
-            yield ("wait", "do_full", t)
+            if mutation != "dP-skips-dO-wait":
+                yield ("wait", "do_full", t)
             if not own_dq and t > 0 and mutation != "dP-skips-dQ-drain":
                 yield ("wait", "dq_empty", t - 1)
             mma("dP", t); commit("dp_full", t)
@@ -125,10 +129,8 @@ def run(T, own_dq, new_order, seed, mutation=None):
             if new_order and mutation != "S-before-dV" and t + 1 < T:
                 yield ("wait", f"q_full{(t + 1) & 1}", (t + 1) >> 1)
                 mma("S", t + 1); commit("s_full", t + 1)
-            yield ("wait", "ds_half", t)
-            mma("dK1", t)
             yield ("wait", "ds_ready", t)
-            mma("dK2", t); commit(f"q_empty{st}", t >> 1)
+            mma("dK", t); commit(f"q_empty{st}", t >> 1)
             next_s_first = (not new_order) and own_dq   # main: d = 64 puts S^T(t+1) before dQ
             if next_s_first and t + 1 < T:
                 yield ("wait", f"q_full{(t + 1) & 1}", (t + 1) >> 1)
@@ -155,10 +157,10 @@ def run(T, own_dq, new_order, seed, mutation=None):
             rd("dO", ("dO", t))
             for w in W:
                 rd(A(w, "lo"), ("P", t))
-        elif kind in ("dK1", "dK2"):
+        elif kind == "dK":
             rd(("Q", t & 1), ("Q", t))
             for w in W:
-                rd(ds_reg(w), {("dS_half", t), ("dS", t)} if kind == "dK1" else ("dS", t))
+                rd(ds_reg(w), ("dS", t))
         elif kind == "dQ":
             for w in W:
                 rd(("smem_dS", w), ("dS", t))
@@ -178,7 +180,6 @@ def run(T, own_dq, new_order, seed, mutation=None):
                 yield ("wait", "dp_full", t)
             rd(B(w, "lo"), ("dP", t)); rd(("Q", st), ("Q", t))
             wr(("smem_dS", w), ("dS_half", t)); wr(ds_reg(w), ("dS_half", t))
-            arrive("ds_half", t, 32)
             yield None
             rd(B(w, "hi"), ("dP", t))
             wr(("smem_dS", w), ("dS", t)); wr(ds_reg(w), ("dS", t))
@@ -216,6 +217,8 @@ def run(T, own_dq, new_order, seed, mutation=None):
                 ready.append(n)
         if pipe_q:
             ready.append("pipe")
+        if "prod" in ready and len(ready) > 1 and rnd.random() >= prod_prob:
+            ready.remove("prod")  # prod_prob < 1 makes loads land late
         if not ready:
             if len(done) == len(procs):
                 return
@@ -246,7 +249,7 @@ ORDERS = {"kernel": True, "earlier": False}
 def test_protocol_is_free_of_deadlock_aliasing_and_hazards(order, d):
     for T in (1, 2, 3, 4, 5, 7):
         for seed in range(60):
-            run(T, own_dq=(d == 64), new_order=ORDERS[order], seed=seed)
+            run(T, own_dq=(d == 64), new_order=ORDERS[order], seed=seed, prod_prob=0.15 if seed % 3 == 0 else 1.0)
 
 
 @pytest.mark.parametrize("mutation, order, d", [
@@ -255,13 +258,15 @@ def test_protocol_is_free_of_deadlock_aliasing_and_hazards(order, d):
     ("dP-skips-dQ-drain", "kernel", 128),         # dP^T(t+1) would overwrite dQ(t) before its drain
     ("dP-skips-dQ-drain", "earlier", 128),
     ("dS-without-dP-wait", "kernel", 64),         # dS phase would read dP^T before it is written
+    ("dP-skips-dO-wait", "kernel", 128),          # dP^T(t) would read a dO tile that has not landed
 ])
 def test_planted_protocol_mistakes_are_caught(mutation, order, d):
     failures = 0
     for T in (2, 3, 4):
         for seed in range(40):
             try:
-                run(T, own_dq=(d == 64), new_order=ORDERS[order], seed=seed, mutation=mutation)
+                run(T, own_dq=(d == 64), new_order=ORDERS[order], seed=seed, mutation=mutation,
+                    prod_prob=0.15 if seed & 1 else 1.0)
             except Err:
                 failures += 1
     assert failures > 0, f"{mutation} went unnoticed"

@@ -160,7 +160,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dp_full = bars + 8;
   uint64_t* p_ready = bars + 9;
   uint64_t* ds_ready = bars + 10;
-  uint64_t* ds_half = bars + 11;  // dS^T of each warpgroup's first 32 query columns is in TMEM
   uint64_t* dq_full = bars + 12;
   uint64_t* dq_empty = bars + 13;
   uint64_t* acc_done = bars + 14;
@@ -211,7 +210,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 256);
     mbar_init(ds_ready, 256);
-    mbar_init(ds_half, 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(acc_done, 1);
@@ -341,21 +339,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // dS^T lives in TMEM as packed bf16 over dP^T, in the same column
         // pattern as P^T: query columns [0,64) at [128,160), [64,128) at
-        // [192,224).  K steps 0, 1, 4, 5 (each warpgroup's first 32 query
-        // columns) go as soon as that half is written; 2, 3, 6, 7 once all of dS is.
-        if (!mbar_wait(ds_half, t & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < BM / 16; ++k)
-          if ((k & 3) < 2)
-            mma_ts(T_DK, T_DP + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_dk,
-                   (t > 0 || k > 0) ? 1u : 0u);
+        // [192,224).  (dK waits for all of it: by the time S^T(t+1) is
+        // queued the elementwise warps have finished both halves, and every
+        // extra barrier check would leave the tensor pipe idle for a
+        // shared-memory round trip.)
         if (!mbar_wait(ds_ready, t & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BM / 16; ++k)
-          if ((k & 3) >= 2)
-            mma_ts(T_DK, T_DP + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_dk, 1u);
+          mma_ts(T_DK, T_DP + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_dk,
+                 (t > 0 || k > 0) ? 1u : 0u);
         mma_commit(&q_empty[st]);
         if (kOwnDQ && t > 0) {  // dQ(t-1) drained from its columns
           if (!mbar_wait(dq_empty, (t - 1) & 1, abort_flag)) { ok = false; break; }
@@ -470,11 +463,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           // packed dS^T of these 8 columns, for the dK MMA (A from TMEM), over
           // dP^T columns this thread has already read
           tmem_st4(T_DP + lane_base + wg * 64 + ch * 16 + cc * 4, w[0], w[1], w[2], w[3]);
-        }
-        if (ch == 0) {  // first half of dS^T in TMEM: the dK MMA may start on it
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(ds_half);
         }
       }
       tmem_wait_st();
