@@ -67,7 +67,7 @@ constexpr int kThreads = 512;
 // kRegsLaunch.
 constexpr int kRegsLaunch = 65536 / kThreads;  // 128
 constexpr int kRegsLow = 80;
-constexpr int kRegsHigh = 2 * kRegsLaunch - kRegsLow;  // 192
+constexpr int kRegsHigh = 2 * kRegsLaunch - kRegsLow;  // 176
 template <int HD>
 constexpr bool kSplitRegs = HD == 128;
 static_assert(kRegsLow % 8 == 0 && kRegsHigh % 8 == 0 && kRegsHigh <= 256, "setmaxnreg operands");
