@@ -553,73 +553,100 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // D = rowsum(dO * O) and L2 = L * log2(e) per padded query row (padding rows:
 // D = 0, L2 = +inf); zeroes the row of the fp32 dQ accumulator.  HD: columns
-// of the accumulator (d); HDV: columns of O and dO (dv).
+// of the accumulator (d); HDV: columns of O and dO (dv).  A row is HDV / 8
+// lanes with 16 bytes of O and of dO each; a warp takes two groups of
+// 32 / (HDV / 8) rows per step, so that every lane has four 16-byte loads in
+// flight (the kernel is short and bound by memory latency as much as by
+// bandwidth).
 template <int HD, int HDV>
 __global__ void __launch_bounds__(256) fa_bwd_pre(const uint16_t* __restrict__ O, const uint16_t* __restrict__ dO,
                                                   const float* __restrict__ L, float* __restrict__ lse2,
                                                   float* __restrict__ delta, float* __restrict__ dq_acc,
                                                   long long rows_pad, int Tq, long long Tq_pad) {
-  constexpr int PER = HDV / 32;  // O / dO elements per lane
-  constexpr int PERQ = HD / 32;  // accumulator elements per lane
-  const int lane = threadIdx.x & 31;
+  constexpr int LPR = HDV / 8;   // lanes per row
+  constexpr int RPG = 32 / LPR;  // rows per group
+  constexpr int UNR = 2;         // groups per warp step
+  constexpr int ZF4 = HD / (4 * LPR);  // float4 of the accumulator row each lane zeroes
+  const int lane = threadIdx.x & 31, sub = lane / LPR, part = lane - sub * LPR;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows_pad;
-       row += warps) {
-    const long long bh = row / Tq_pad;
-    const long long q = row - bh * Tq_pad;
-    float dot = 0.f;
-    if (q < Tq) {
-      const long long src = (bh * Tq + q) * HDV + lane * PER;
-      if (PER == 4) {
-        const uint2 a = *reinterpret_cast<const uint2*>(O + src);
-        const uint2 g = *reinterpret_cast<const uint2*>(dO + src);
-        const uint32_t aw[2] = {a.x, a.y}, gw[2] = {g.x, g.y};
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  for (long long base = wid * (RPG * UNR); base < rows_pad; base += warps * (RPG * UNR)) {
+    uint4 a[UNR], g[UNR];
+    long long row[UNR], src_row[UNR];
+    bool real[UNR];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          dot += __uint_as_float(aw[e] << 16) * __uint_as_float(gw[e] << 16);
-          dot += __uint_as_float(aw[e] & 0xffff0000u) * __uint_as_float(gw[e] & 0xffff0000u);
-        }
-      } else {
-        const uint32_t a = *reinterpret_cast<const uint32_t*>(O + src);
-        const uint32_t g = *reinterpret_cast<const uint32_t*>(dO + src);
-        dot += __uint_as_float(a << 16) * __uint_as_float(g << 16);
-        dot += __uint_as_float(a & 0xffff0000u) * __uint_as_float(g & 0xffff0000u);
+    for (int u = 0; u < UNR; ++u) {
+      row[u] = base + u * RPG + sub;
+      const long long bh = row[u] / Tq_pad;
+      const long long q = row[u] - bh * Tq_pad;
+      real[u] = row[u] < rows_pad && q < Tq;
+      src_row[u] = bh * Tq + q;
+      a[u] = g[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (real[u]) {
+        a[u] = *reinterpret_cast<const uint4*>(O + src_row[u] * HDV + part * 8);
+        g[u] = *reinterpret_cast<const uint4*>(dO + src_row[u] * HDV + part * 8);
       }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-    if (lane == 0) {
-      delta[row] = dot;
-      lse2[row] = q < Tq ? L[bh * Tq + q] * 1.4426950408889634f : __int_as_float(0x7f800000);
+    for (int u = 0; u < UNR; ++u) {
+      const uint32_t aw[4] = {a[u].x, a[u].y, a[u].z, a[u].w}, gw[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        dot += __uint_as_float(aw[e] << 16) * __uint_as_float(gw[e] << 16);
+        dot += __uint_as_float(aw[e] & 0xffff0000u) * __uint_as_float(gw[e] & 0xffff0000u);
+      }
+#pragma unroll
+      for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      if (row[u] < rows_pad) {
+        if (part == 0) {
+          delta[row[u]] = dot;
+          lse2[row[u]] = real[u] ? L[src_row[u]] * 1.4426950408889634f : __int_as_float(0x7f800000);
+        }
+        float4* acc = reinterpret_cast<float4*>(dq_acc + row[u] * HD) + part * ZF4;
+#pragma unroll
+        for (int z = 0; z < ZF4; ++z) acc[z] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
-    float* acc = dq_acc + row * HD + lane * PERQ;
-    if (PERQ == 4)
-      *reinterpret_cast<float4*>(acc) = make_float4(0.f, 0.f, 0.f, 0.f);
-    else
-      *reinterpret_cast<float2*>(acc) = make_float2(0.f, 0.f);
   }
 }
 
-// dQ = bf16(scale * accumulator), 8 elements per thread.
+// dQ = bf16(scale * accumulator).  A row is HD / 8 lanes with 8 fp32 each;
+// a warp takes two groups of 32 / (HD / 8) rows per step (four 16-byte loads
+// in flight per lane).
 template <int HD>
 __global__ void __launch_bounds__(256) fa_dq_cast(const float* __restrict__ dq_acc, uint16_t* __restrict__ dQ,
-                                                  long long n_vec, int Tq, long long Tq_pad, float scale) {
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < n_vec; v += stride) {
-    const long long e = v * 8;
-    const long long row = e / HD;
-    const int col = (int)(e - row * HD);
-    const long long bh = row / Tq;
-    const long long q = row - bh * Tq;
-    const float* src = dq_acc + (bh * Tq_pad + q) * HD + col;
-    const float4 a = *reinterpret_cast<const float4*>(src);
-    const float4 c = *reinterpret_cast<const float4*>(src + 4);
-    uint4 o;
-    o.x = pack_bf16x2(a.x * scale, a.y * scale);
-    o.y = pack_bf16x2(a.z * scale, a.w * scale);
-    o.z = pack_bf16x2(c.x * scale, c.y * scale);
-    o.w = pack_bf16x2(c.z * scale, c.w * scale);
-    *reinterpret_cast<uint4*>(dQ + e) = o;
+                                                  long long q_rows, int Tq, long long Tq_pad, float scale) {
+  constexpr int LPR = HD / 8;
+  constexpr int RPG = 32 / LPR;
+  constexpr int UNR = 2;
+  const int lane = threadIdx.x & 31, sub = lane / LPR, part = lane - sub * LPR;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  for (long long base = wid * (RPG * UNR); base < q_rows; base += warps * (RPG * UNR)) {
+    float4 x[UNR], y[UNR];
+    long long row[UNR];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      row[u] = base + u * RPG + sub;
+      x[u] = y[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (row[u] < q_rows) {
+        const long long bh = row[u] / Tq;
+        const float* src = dq_acc + (bh * Tq_pad + (row[u] - bh * Tq)) * HD + part * 8;
+        x[u] = *reinterpret_cast<const float4*>(src);
+        y[u] = *reinterpret_cast<const float4*>(src + 4);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      if (row[u] >= q_rows) continue;
+      uint4 o;
+      o.x = pack_bf16x2(x[u].x * scale, x[u].y * scale);
+      o.y = pack_bf16x2(x[u].z * scale, x[u].w * scale);
+      o.z = pack_bf16x2(y[u].x * scale, y[u].y * scale);
+      o.w = pack_bf16x2(y[u].z * scale, y[u].w * scale);
+      *reinterpret_cast<uint4*>(dQ + row[u] * HD + part * 8) = o;
+    }
   }
 }
 
@@ -724,7 +751,7 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
   if (stages & FA_BWD_PRE) {
   auto pre = pr.d == 64 ? (pr.dv == 64 ? fa_bwd_pre<64, 64> : fa_bwd_pre<64, 128>)
                         : (pr.dv == 64 ? fa_bwd_pre<128, 64> : fa_bwd_pre<128, 128>);
-  pre<<<grid_for(rows_pad, 8), 256, 0, stream>>>(static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), L,
+  pre<<<grid_for(rows_pad, 8 * 2 * (32 / (pr.dv / 8))), 256, 0, stream>>>(static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), L,
                                                  lse2, delta, dq_acc, rows_pad, pr.Tq, pr.Tq_pad());
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -772,13 +799,13 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
 
   // 3. dQ cast
   if (!(stages & FA_BWD_CAST)) return cudaSuccess;
-  const long long n_vec = q_rows * pr.d / 8;
+  const int rows_per_block = 8 * 2 * (32 / (pr.d / 8));  // 8 warps, two row groups each
   if (pr.d == 64)
-    fa_dq_cast<64><<<grid_for(n_vec, 256), 256, 0, stream>>>(dq_acc, static_cast<uint16_t*>(dQ), n_vec, pr.Tq,
-                                                             pr.Tq_pad(), pr.scale);
+    fa_dq_cast<64><<<grid_for(q_rows, rows_per_block), 256, 0, stream>>>(dq_acc, static_cast<uint16_t*>(dQ), q_rows,
+                                                                         pr.Tq, pr.Tq_pad(), pr.scale);
   else
-    fa_dq_cast<128><<<grid_for(n_vec, 256), 256, 0, stream>>>(dq_acc, static_cast<uint16_t*>(dQ), n_vec, pr.Tq,
-                                                              pr.Tq_pad(), pr.scale);
+    fa_dq_cast<128><<<grid_for(q_rows, rows_per_block), 256, 0, stream>>>(dq_acc, static_cast<uint16_t*>(dQ),
+                                                                          q_rows, pr.Tq, pr.Tq_pad(), pr.scale);
   e = cudaGetLastError();
   if (e == cudaSuccess) ++*launches;
   return e;
