@@ -74,6 +74,31 @@ def test_small_shapes_full_parity(fa, shape):
     assert_close("dV", got["dV"], dV)
 
 
+# Without a causal mask the forward splits a short last round of query-tile
+# pairs into single-tile work items (the second half of a pair then belongs to
+# another item, or lies past the last row).  Shapes: 6 pairs with an odd tile
+# count (the last pair's second half is past Tq), and 170 pairs (18 left over
+# after one round of 152 SMs).
+SPLIT = [
+    (1, 3, 1, 300, 257, 64),
+    (1, 85, 5, 512, 130, 64),
+]
+
+
+@pytest.mark.parametrize("shape", SPLIT, ids=lambda s: "x".join(map(str, s)))
+def test_forward_single_tile_items(fa, shape):
+    B, Hq, Hkv, Tq, Tk, d = shape
+    Q, K, V, dO = make_custom(B, Hq, Hkv, Tq, Tk, d, False, seed=sum(shape) + 5)
+    got = run_gpu(fa, Q, K, V, dO, False)
+    O, L = oracle.forward(Q, K, V, False)
+    dQ, dK, dV, _ = oracle.backward(Q, K, V, dO, False)
+    assert_close("O", got["O"], O)
+    assert_L_close("L", got["L"], L)
+    assert_close("dQ", got["dQ"], dQ)
+    assert_close("dK", got["dK"], dK)
+    assert_close("dV", got["dV"], dV)
+
+
 @pytest.mark.parametrize("Tq", [32, 300])
 def test_appended_queries_over_long_prefix(fa, Tq):
     """Queries appended after an ~8000-token prefix (Tk = 8000 + 32, 32 query / 8

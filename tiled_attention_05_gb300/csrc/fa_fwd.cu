@@ -133,7 +133,8 @@ struct FwdParams {
   int kv_tiles;
   int n_bh;            // B * Hq
   int n_pairs;         // query-tile pairs per (batch, head)
-  long long n_items;   // n_bh * n_pairs
+  long long n_full;    // work items that are pairs of query tiles
+  long long n_items;   // all work items: n_full pairs, then single query tiles
   float scale_log2;  // scale * log2(e)
   int test_withhold_q;  // test build only: never issue the Q loads (every wait then times out)
 };
@@ -167,24 +168,35 @@ struct FwdItem {
   int bh, q0, bkv;
   int kb[2], ke[2];  // key-tile range of tile A and tile B
   int ub, ue;        // their union, loaded once
+  bool single;       // tile B is not part of the item (its rows belong to another item)
 };
 
 // The n-th item of this CTA, or false past its last.  Items are numbered
 // heaviest causal rows first (the pair index slowest); round n of the grid
 // takes items [n * G, n * G + G), CTA c the c-th of them in even rounds and
 // the (G - 1 - c)-th in odd ones, so each CTA's heavy and light items pair up.
+// Past n_full, every pair is split into two single-tile items (tile B empty),
+// which spreads a short last round of equal-weight items over twice as many
+// CTAs.
 template <bool CAUSAL, bool WINDOW>
 __device__ __forceinline__ bool fwd_item(const FwdParams& p, int n, FwdItem* it) {
   const long long G = gridDim.x, c = blockIdx.x;
   const long long k = n * G + ((n & 1) ? G - 1 - c : c);
   if (k >= p.n_items) return false;
-  const int y = (int)(k / p.n_bh);
-  it->bh = (int)(k - (long long)y * p.n_bh);
+  const bool single = k >= p.n_full;
+  it->single = single;
+  const long long kp = single ? p.n_full + ((k - p.n_full) >> 1) : k;  // the pair
+  const int y = (int)(kp / p.n_bh);
+  it->bh = (int)(kp - (long long)y * p.n_bh);
   const int b = it->bh / p.Hq, h = it->bh - b * p.Hq;
-  it->q0 = (p.n_pairs - 1 - y) * (2 * BM);
+  it->q0 = (p.n_pairs - 1 - y) * (2 * BM) + (single ? (int)((k - p.n_full) & 1) * BM : 0);
   it->bkv = b * p.Hkv + h / p.G;
   kv_range_for<CAUSAL, WINDOW>(p, it->q0, &it->kb[0], &it->ke[0]);
-  kv_range_for<CAUSAL, WINDOW>(p, it->q0 + BM, &it->kb[1], &it->ke[1]);
+  if (single) {
+    it->kb[1] = it->ke[1] = 0;
+  } else {
+    kv_range_for<CAUSAL, WINDOW>(p, it->q0 + BM, &it->kb[1], &it->ke[1]);
+  }
   // Tile B's rows follow tile A's, so B's range starts and ends no earlier
   // than A's, and starts no later than A's end: the union has no gap and
   // every key tile in it is needed by A or B.
@@ -549,7 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++no;
         tc_fence_after();
       }
-      if (!ok || qx0 >= p.Tq) continue;  // (a tile past the last row has nothing to write)
+      // (a tile past the last row, or tile B of a single-tile item, has nothing to write)
+      if (!ok || qx0 >= p.Tq || (x == 1 && it.single)) continue;
       const bool row_ok = i < p.Tq;
       if (row_ok) p.L[(size_t)it.bh * p.Tq + i] = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : NEG_INF;
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -626,7 +639,13 @@ cudaError_t launch_fwd_t(const fa::Problem& pr, const CUtensorMap& mq, const CUt
   p.kv_tiles = pr.kv_tiles();
   p.n_bh = pr.B * pr.Hq;
   p.n_pairs = (pr.q_tiles() + 1) / 2;
-  p.n_items = (long long)p.n_bh * p.n_pairs;
+  const long long n_pair_items = (long long)p.n_bh * p.n_pairs;
+  // Without a causal mask every item has the same work.  A last round with at
+  // most half as many items as SMs then runs them as single tiles on twice
+  // as many SMs (a tile alone takes ~0.65 of a pair's time: no ping-pong).
+  const long long r = n_pair_items % sms;
+  p.n_full = (!pr.causal && r > 0 && 2 * r <= sms) ? n_pair_items - r : n_pair_items;
+  p.n_items = p.n_full + 2 * (n_pair_items - p.n_full);
   p.scale_log2 = pr.scale * 1.4426950408889634f;
   p.test_withhold_q = fa::test_withhold() == fa::kWithholdFwdQ;
   const int grid = (int)(p.n_items < sms ? p.n_items : sms);
