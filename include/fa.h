@@ -90,7 +90,10 @@ FA_API fa_status fa_forward(const fa_dims* dims, const void* Q, const void* K, c
 
 /* Size in bytes of the scratch buffer fa_backward needs: an fp32 dQ
  * accumulator [B, Hq, ceil(Tq/128)*128, d] plus two fp32 row vectors
- * (D and log2-scaled L) of B*Hq*ceil(Tq/128)*128 entries, plus alignment. */
+ * (D and log2-scaled L) of B*Hq*ceil(Tq/128)*128 entries, plus alignment;
+ * without a causal mask also room for the partial dK / dV
+ * of up to min(B*Hkv*ceil(Tk/128), 128) key tiles whose work is split in two
+ * (fp32, 2 x 128 x (d + dv) each) and a 4-byte counter per such tile. */
 FA_API size_t fa_backward_workspace_bytes(const fa_dims* dims);
 
 /* Backward pass from O, L of fa_forward (same dims) and the upstream gradient
@@ -103,7 +106,8 @@ FA_API fa_status fa_backward(const fa_dims* dims, const void* Q, const void* K, 
 
 /* The backward in separately launchable stages, for callers that interleave
  * other work or time the stages: bit 0 = preprocess (D = rowsum(dO * O), L in
- * log2 units, zero the dQ accumulator in `workspace`), bit 1 = the main
+ * log2 units, zero the dQ accumulator and the split-tile counters in
+ * `workspace`), bit 1 = the main
  * recompute kernel (dK, dV, dQ accumulation), bit 2 = dQ cast.  Stages must run
  * in order on the same workspace; fa_backward is fa_backward_stages(..., 7). */
 enum { FA_BWD_PRE = 1, FA_BWD_MAIN = 2, FA_BWD_CAST = 4, FA_BWD_ALL = 7 };

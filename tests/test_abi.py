@@ -96,12 +96,17 @@ def test_backward_workspace_validation():
 
 
 def test_workspace_size_formula():
-    for B, Hq, Tq, dd in ((1, 1, 256, 64), (2, 32, 8192, 128), (1, 32, 4096, 128), (3, 5, 1, 64)):
-        d = dims(B=B, Hq=Hq, Hkv=1, Tq=Tq, Tk=50, d=dd, dv=dd)
+    up = lambda x: (x + 255) // 256 * 256
+    for B, Hq, Tq, Tk, dd, causal, window in ((1, 1, 256, 50, 64, 0, 0), (2, 32, 8192, 8192, 128, 1, 0),
+                                              (1, 32, 4096, 8032, 128, 0, 0), (3, 5, 1, 50, 64, 0, 0),
+                                              (1, 32, 8192, 8192, 128, 1, 2080), (40, 8, 128, 9000, 64, 0, 0)):
+        d = dims(B=B, Hq=Hq, Hkv=1, Tq=Tq, Tk=Tk, d=dd, dv=dd, causal=causal, window=window)
         rows = B * Hq * ((Tq + 127) // 128) * 128
-        up = lambda x: (x + 255) // 256 * 256
-        want = up(up(up(rows * dd * 4) + rows * 4) + rows * 4)
-        assert fa.fa_backward_workspace_bytes(d) == want
+        base = up(up(up(rows * dd * 4) + rows * 4) + rows * 4)
+        # key tiles that may be split in two: equal-work items only (no causal mask)
+        cap = min(B * 1 * ((Tk + 127) // 128), 128) if not causal else 0
+        want = up(base + cap * 2 * 128 * (2 * dd) * 4) + cap * 4
+        assert fa.fa_backward_workspace_bytes(d) == up(want)
     assert fa.fa_backward_workspace_bytes(dims(Hq=3, Hkv=2)) == 0
 
 

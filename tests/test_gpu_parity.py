@@ -74,19 +74,26 @@ def test_small_shapes_full_parity(fa, shape):
     assert_close("dV", got["dV"], dV)
 
 
-# Without a causal mask the forward splits a short last round of query-tile
-# pairs into single-tile work items (the second half of a pair then belongs to
-# another item, or lies past the last row).  Shapes: 6 pairs with an odd tile
-# count (the last pair's second half is past Tq), and 170 pairs (18 left over
-# after one round of 152 SMs).
+# Without a causal mask both kernels split a short last round of work items:
+# the forward into single query tiles (the second half of a pair then belongs
+# to another item, or lies past the last row), the backward into two halves
+# of a key tile's query tiles whose dK / dV are added.  Shapes: 6 pairs with
+# an odd tile count (the last pair's second half is past Tq) and 3 key tiles
+# of 9 tiles each; 170 pairs (18 left over after one round of 152 SMs) and 10
+# key tiles of 68; one query tile per key tile (one half of each backward
+# item has no tile); 160 key tiles (152 whole items, 8 split) at d = 64; 9
+# key tiles at d = 128.
 SPLIT = [
     (1, 3, 1, 300, 257, 64),
     (1, 85, 5, 512, 130, 64),
+    (1, 1, 1, 100, 300, 64),
+    (1, 1, 1, 64, 20480, 64),
+    (1, 2, 1, 200, 1100, 128),
 ]
 
 
 @pytest.mark.parametrize("shape", SPLIT, ids=lambda s: "x".join(map(str, s)))
-def test_forward_single_tile_items(fa, shape):
+def test_split_work_items(fa, shape):
     B, Hq, Hkv, Tq, Tk, d = shape
     Q, K, V, dO = make_custom(B, Hq, Hkv, Tq, Tk, d, False, seed=sum(shape) + 5)
     got = run_gpu(fa, Q, K, V, dO, False)

@@ -101,8 +101,11 @@ struct BwdCfg {
 // thread's key row r, the warpgroup's half of the columns (wg), times `mul`,
 // as bf16 into a 128-row, 128B-swizzled staging tile for the TMA store.
 // `have` is false when the CTA saw no query tile: the rows are zero.
+// `add` (optional): the same row's partial sums from the other half of a
+// split item, this warpgroup's columns, added before the scaling.
 template <int W>
-__device__ __forceinline__ void stage_rows_bf16(uint32_t src, uint8_t* stage, int r, int wg, float mul, bool have) {
+__device__ __forceinline__ void stage_rows_bf16(uint32_t src, uint8_t* stage, int r, int wg, float mul, bool have,
+                                                const float* add = nullptr) {
   constexpr int HALF = W / 2;
 #pragma unroll
   for (int c = 0; c < HALF / 32; ++c) {
@@ -113,6 +116,16 @@ __device__ __forceinline__ void stage_rows_bf16(uint32_t src, uint8_t* stage, in
     } else {
 #pragma unroll
       for (int e = 0; e < 32; ++e) v[e] = 0u;
+    }
+    if (add) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(add + c * 32) + q);
+        v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) + a.x);
+        v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + a.y);
+        v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + a.z);
+        v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + a.w);
+      }
     }
     const int col0 = wg * HALF + c * 32;  // first column of this chunk
 #pragma unroll
@@ -128,6 +141,30 @@ __device__ __forceinline__ void stage_rows_bf16(uint32_t src, uint8_t* stage, in
   }
 }
 
+// This row's fp32 sums of one accumulator (W columns in TMEM at src, this
+// warpgroup's half of them) into a split item's partial area (zeros if the
+// half saw no tile).
+template <int W>
+__device__ __forceinline__ void write_partial(uint32_t src, float* dst, bool have) {
+  constexpr int HALF = W / 2;
+#pragma unroll
+  for (int c = 0; c < HALF / 32; ++c) {
+    uint32_t v[32];
+    if (have) {
+      tmem_ld32(src + c * 32, v);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = 0u;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      __stcg(reinterpret_cast<float4*>(dst + c * 32) + q,
+             make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                         __uint_as_float(v[4 * q + 3])));
+  }
+}
+
 struct BwdParams {
   const float* lse2;
   const float* delta;
@@ -138,6 +175,14 @@ struct BwdParams {
   long long Tq_pad;
   float scale_log2, scale;
   int test_withhold_do;  // test build only: never issue the dO loads (the CTA's waits then time out)
+  // Split items: the last n_split items of the grid order run as two CTAs
+  // each (CTAs n_whole + 2 s and n_whole + 2 s + 1 for item n_whole + s),
+  // each walking half of the item's query tiles; the halves' fp32 dK / dV
+  // meet in `part`, and whichever half finishes second adds the other's and
+  // stores them (split_counters, zeroed by fa_bwd_pre, tell them apart).
+  int n_whole, n_split;
+  float* part;                    // [n_split][2 halves][128 key rows][d + dv]
+  unsigned int* split_counters;   // [n_split]
 };
 
 // WINDOW (causal only): the sliding-window terms are compiled in only where
@@ -166,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = bars + 15;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile unsigned int* split_seen = reinterpret_cast<volatile unsigned int*>(tmem_slot + 2);  // halves counted before
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // One linear grid in super-batches of sb_groups (batch, kv head) groups;
@@ -176,9 +222,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // groups' Q, dO and fp32 dQ accumulator are live at a time, so they stay in
   // L2.  (One group at a time keeps even less live, but its late heavy CTAs
   // make the causal step ~12% longer.)
+  // Split items exist only without a causal mask (equal-work items); the
+  // causal instances compile none of their code.
+  constexpr bool SPLIT = !CAUSAL;
+  int item = blockIdx.x, split = -1, half = 0;
+  if (SPLIT && item >= p.n_whole) {
+    split = (item - p.n_whole) >> 1;
+    half = (item - p.n_whole) & 1;
+    item = p.n_whole + split;
+  }
   const int per_sb = p.sb_groups * p.kv_tiles;
-  const int sb = blockIdx.x / per_sb;
-  const int in_sb = blockIdx.x - sb * per_sb;
+  const int sb = item / per_sb;
+  const int in_sb = item - sb * per_sb;
   const int n = in_sb / p.sb_groups;  // key tile
   const int bkv = sb * p.sb_groups + (in_sb - n * p.sb_groups);
   const int b = bkv / p.Hkv, hk = bkv - b * p.Hkv;
@@ -195,7 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   const int n_m = max(0, m_end - m_begin);
-  const int T = p.G * n_m;  // tiles this CTA walks
+  const int T_item = p.G * n_m;  // the item's tiles
+  // this CTA's tiles: [t0, t0 + T) of the item's
+  const int t0 = split >= 0 && half ? T_item / 2 : 0;
+  const int T = split >= 0 ? (half ? T_item - T_item / 2 : T_item / 2) : T_item;
 
   if (threadIdx.x == 0) {
     *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;
@@ -252,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int last_q[2] = {-1, -1}, last_do = -1;
       for (int t = 0; t < T; ++t) {
         const int st = t & 1, u = t >> 1;
-        const int g = t / n_m, m = m_begin + (t - g * n_m);
+        const int g = (t0 + t) / n_m, m = m_begin + ((t0 + t) - g * n_m);
         const int bh = b * p.Hq + hk * p.G + g;
         if (!mbar_wait(&q_empty[st], (u & 1) ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(&q_full[st], C::QK_TILE + 1024);
@@ -376,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = run;
     for (int t = 0; ok && t < T; ++t) {
       const int st = t & 1, u = t >> 1;
-      const int g = t / n_m, m = m_begin + (t - g * n_m);
+      const int g = (t0 + t) / n_m, m = m_begin + ((t0 + t) - g * n_m);
       const int q0 = m * BM;
       const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE + st * 512);
       const float* del_s = reinterpret_cast<const float*>(smem + C::OFF_DELTA + st * 512);
@@ -477,8 +535,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const bool mine = (T == 0 || ok) && *abort_flag == 0;
     if (named_bar_and(1, 256, mine)) {
-      stage_rows_bf16<HDV>(T_DV + lane_base + wg * (HDV / 2), smem + C::OFF_DV_STAGE, r, wg, 1.f, T > 0);
-      stage_rows_bf16<HD>(T_DK + lane_base + wg * (HD / 2), smem + C::OFF_DK_STAGE, r, wg, p.scale, T > 0);
+      // A split item's halves: each writes its fp32 sums to the partial area
+      // and counts itself in; the one that comes second adds the other's sums
+      // to its own and stores the item's dV and dK.  Neither waits for the other.
+      const float* other = nullptr;
+      bool finish = true;
+      if (split >= 0) {
+        float* own = p.part + (((size_t)split * 2 + half) * BN + r) * (HD + HDV);
+        write_partial<HDV>(T_DV + lane_base + wg * (HDV / 2), own + wg * (HDV / 2), T > 0);
+        write_partial<HD>(T_DK + lane_base + wg * (HD / 2), own + HDV + wg * (HD / 2), T > 0);
+        __threadfence();
+        named_bar_sync(3, 256);
+        if (warp == 4 && lane == 0) *split_seen = atomicAdd(&p.split_counters[split], 1u);
+        named_bar_sync(3, 256);
+        finish = *split_seen == 1u;
+        if (finish) {
+          __threadfence();
+          other = p.part + (((size_t)split * 2 + (half ^ 1)) * BN + r) * (HD + HDV);
+        }
+      }
+      if (!finish) goto epilogue_done;
+      stage_rows_bf16<HDV>(T_DV + lane_base + wg * (HDV / 2), smem + C::OFF_DV_STAGE, r, wg, 1.f, T > 0,
+                           other ? other + wg * (HDV / 2) : nullptr);
+      stage_rows_bf16<HD>(T_DK + lane_base + wg * (HD / 2), smem + C::OFF_DK_STAGE, r, wg, p.scale, T > 0,
+                          other ? other + HDV + wg * (HD / 2) : nullptr);
       fence_async_smem();
       named_bar_sync(2, 256);
       if (warp == 4 && lane == 0) {
@@ -494,6 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_wait0();
       }
     }
+  epilogue_done:;
   } else {
     // ------------------------------------------------------------ dQ warpgroup
     if (kSplitRegs<HD>) setmaxnreg_inc<kRegsHigh>();
@@ -510,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NCH = HD / 32;  // 32-column chunks per tile
     bool ok = run;
     for (int t = 0; ok && t < T; ++t) {
-      const int g = t / n_m, m = m_begin + (t - g * n_m);
+      const int g = (t0 + t) / n_m, m = m_begin + ((t0 + t) - g * n_m);
       const int bh = b * p.Hq + hk * p.G + g;
       if (!__all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
@@ -552,7 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // D = rowsum(dO * O) and L2 = L * log2(e) per padded query row (padding rows:
-// D = 0, L2 = +inf); zeroes the row of the fp32 dQ accumulator.  HD: columns
+// D = 0, L2 = +inf); zeroes the row of the fp32 dQ accumulator (and the main
+// kernel's split-item counters).  HD: columns
 // of the accumulator (d); HDV: columns of O and dO (dv).  A row is HDV / 8
 // lanes with 16 bytes of O and of dO each; a warp takes two groups of
 // 32 / (HDV / 8) rows per step, so that every lane has four 16-byte loads in
@@ -562,7 +644,10 @@ template <int HD, int HDV>
 __global__ void __launch_bounds__(256) fa_bwd_pre(const uint16_t* __restrict__ O, const uint16_t* __restrict__ dO,
                                                   const float* __restrict__ L, float* __restrict__ lse2,
                                                   float* __restrict__ delta, float* __restrict__ dq_acc,
+                                                  unsigned int* __restrict__ split_counters, int n_counters,
                                                   long long rows_pad, int Tq, long long Tq_pad) {
+  if (blockIdx.x == 0)
+    for (int c = threadIdx.x; c < n_counters; c += blockDim.x) split_counters[c] = 0u;
   constexpr int LPR = HDV / 8;   // lanes per row
   constexpr int RPG = 32 / LPR;  // rows per group
   constexpr int UNR = 2;         // groups per warp step
@@ -669,7 +754,8 @@ cudaError_t launch_main_t(const fa::Problem& pr, const CUtensorMap* maps, const 
     if (e != cudaSuccess) return e;
     if (fa_attr.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   }
-  dim3 grid((unsigned)((long long)pr.B * pr.Hkv * pr.kv_tiles()));  // within int range (checked by the API)
+  // one CTA per item, two per split item (within int range: checked by the API, n_split <= kMaxSplitItems)
+  dim3 grid((unsigned)(bp.n_whole + 2 * bp.n_split));
   fa_bwd_main<HD, HDV, CAUSAL, WINDOW><<<grid, kThreads, C::SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
                                                                maps[6], bp);
   return cudaGetLastError();
@@ -712,8 +798,29 @@ BwdWorkspace backward_workspace_layout(const Problem& p) {
   w.dq_acc = 0;
   w.lse2 = up(w.dq_acc + rows * p.d * sizeof(float));
   w.delta = up(w.lse2 + rows * sizeof(float));
-  w.total = up(w.delta + rows * sizeof(float));
+  w.part = up(w.delta + rows * sizeof(float));
+  // Items have equal work without a causal mask: then a short last round may
+  // be split (up to kMaxSplitItems items).  (With a window the last key
+  // tiles of each head are lighter, and splitting did not pay.)
+  const long long n_items = (long long)p.B * p.Hkv * p.kv_tiles();
+  w.split_cap = !p.causal ? (int)(n_items < kMaxSplitItems ? n_items : kMaxSplitItems) : 0;
+  w.counters = up(w.part + (size_t)w.split_cap * 2 * kTile * (p.d + p.dv) * sizeof(float));
+  w.total = up(w.counters + (size_t)w.split_cap * sizeof(unsigned int));
   return w;
+}
+
+// Items of the backward main kernel run as two halves (each half walks half
+// of the item's query tiles and the halves' dK / dV are added): the last
+// n_items mod sms items, where items have equal work and that last round
+// fills at most half of the SMs, so its halves run on twice as many SMs.
+int backward_split_items(const Problem& p, int split_cap) {
+  int dev = 0, sms = 0;
+  if (split_cap <= 0 || cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return 0;
+  const long long n_items = (long long)p.B * p.Hkv * p.kv_tiles();
+  const long long r = n_items % sms;
+  return (r > 0 && 2 * r <= sms && r <= split_cap) ? (int)r : 0;
 }
 
 cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, const void* V, const void* O,
@@ -744,6 +851,8 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
   float* dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
   float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
   float* delta = reinterpret_cast<float*>(ws + w.delta);
+  float* part = reinterpret_cast<float*>(ws + w.part);
+  unsigned int* split_counters = reinterpret_cast<unsigned int*>(ws + w.counters);
   const long long rows_pad = (long long)pr.B * pr.Hq * pr.Tq_pad();
 
   cudaError_t e = cudaSuccess;
@@ -752,7 +861,8 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
   auto pre = pr.d == 64 ? (pr.dv == 64 ? fa_bwd_pre<64, 64> : fa_bwd_pre<64, 128>)
                         : (pr.dv == 64 ? fa_bwd_pre<128, 64> : fa_bwd_pre<128, 128>);
   pre<<<grid_for(rows_pad, 8 * 2 * (32 / (pr.dv / 8))), 256, 0, stream>>>(static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), L,
-                                                 lse2, delta, dq_acc, rows_pad, pr.Tq, pr.Tq_pad());
+                                                 lse2, delta, dq_acc, split_counters, w.split_cap, rows_pad, pr.Tq,
+                                                 pr.Tq_pad());
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++*launches;
@@ -788,6 +898,10 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
   bp.scale = pr.scale;
   bp.scale_log2 = pr.scale * 1.4426950408889634f;
   bp.test_withhold_do = fa::test_withhold() == fa::kWithholdBwdDO;
+  bp.n_split = backward_split_items(pr, w.split_cap);
+  bp.n_whole = (int)((long long)pr.B * pr.Hkv * pr.kv_tiles()) - bp.n_split;
+  bp.part = part;
+  bp.split_counters = split_counters;
   if (pr.d == 64)
     e = pr.dv == 64 ? launch_main_dims<64, 64>(pr, maps, bp, stream) : launch_main_dims<64, 128>(pr, maps, bp, stream);
   else

@@ -68,9 +68,16 @@ inline int super_batch_groups(int n_groups, int kv_tiles, int sms) {
   return n_groups;
 }
 
-// Workspace carve-up of fa_backward (byte offsets, 256-aligned).
+// Work items of the backward main kernel that may be split in two (see
+// backward_split_items); the workspace holds their fp32 partial dK / dV.
+constexpr int kMaxSplitItems = 128;
+
+// Workspace carve-up of fa_backward (byte offsets, 256-aligned).  `part` and
+// `counters` (the split items' partial dK / dV and their finish counters)
+// are empty when no item can be split (with a causal mask).
 struct BwdWorkspace {
-  size_t dq_acc, lse2, delta, total;
+  size_t dq_acc, lse2, delta, part, counters, total;
+  int split_cap;  // items the partial area has room for
 };
 BwdWorkspace backward_workspace_layout(const Problem& p);
 
