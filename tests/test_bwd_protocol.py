@@ -25,8 +25,16 @@ Two issue orders are checked. One is the kernel's: S^T(t+1) right after
 dV(t), with dS^T packed over the dP^T columns the elementwise warps have
 already read. The other is the kernel's earlier order, kept as a second
 known-good protocol: S^T(t+1) after dK(t) at d = 64 and after dQ(t) at
-d = 128, with dS^T packed into S^T's columns. Planted protocol mistakes must
-each be caught, so the model is known to be able to fail.
+d = 128, with dS^T packed into S^T's columns.
+
+At d = dv = 64 the kernel also runs with deeper rings (3 Q slots, 2 dO
+slots) and lets other roles vouch for three of the issuing thread's checks:
+one elementwise thread checks Q(t+1) before it arrives on p_ready(t) and
+dO(t+1) before it arrives on ds_ready(t), and the dQ warps arrive on
+ds_ready(t+1) once they have drained dQ(t) (ds_ready then counts 384), so
+the thread waits only for p_ready and ds_ready. That protocol is checked
+too. Planted protocol mistakes must each be caught, so the model is known
+to be able to fail.
 """
 import random
 
@@ -35,15 +43,23 @@ import pytest
 # Arrival counts the kernel initialises its barriers with (q_full / q_empty
 # are two-slot rings; p_ready and ds_ready take every elementwise thread,
 # dq_empty every dQ thread).
-CNT = dict(kv_full=1, q_full0=1, q_full1=1, q_empty0=1, q_empty1=1, do_full=1, do_empty=1, s_full=1, dp_full=1,
-           p_ready=256, ds_ready=256, dq_full=1, dq_empty=128, acc_done=1)
+def counts(nq, ndo, vouch):
+    c = dict(kv_full=1, s_full=1, dp_full=1, p_ready=256, ds_ready=256 + (128 if vouch else 0), dq_full=1,
+             dq_empty=128, acc_done=1)
+    for i in range(nq):
+        c[f"q_full{i}"] = c[f"q_empty{i}"] = 1
+    for i in range(ndo):
+        c[f"do_full{i}"] = c[f"do_empty{i}"] = 1
+    return c
 
 
 class Err(Exception):
     """A protocol violation found in one interleaving."""
 
 
-def run(T, own_dq, new_order, seed, mutation=None, prod_prob=1.0):
+def run(T, own_dq, new_order, seed, mutation=None, prod_prob=1.0, vouch=False):
+    nq, ndo = (3, 2) if vouch else (2, 1)
+    CNT = counts(nq, ndo, vouch)
     rnd = random.Random(seed)
     comp = {b: 0 for b in CNT}
     cur = {b: 0 for b in CNT}
@@ -92,16 +108,17 @@ def run(T, own_dq, new_order, seed, mutation=None, prod_prob=1.0):
         wr("K", "K")
         arrive("kv_full", 0, 1)
         for t in range(T):
-            st, u = t & 1, t >> 1
+            st, u = t % nq, t // nq
             if u >= 1:
                 yield ("wait", f"q_empty{st}", u - 1)
             wr(("Q", st), ("Q", t))
             arrive(f"q_full{st}", u, 1)
             yield None
-            if t >= 1:
-                yield ("wait", "do_empty", t - 1)
-            wr("dO", ("dO", t))
-            arrive("do_full", t, 1)
+            so, uo = t % ndo, t // ndo
+            if uo >= 1:
+                yield ("wait", f"do_empty{so}", uo - 1)
+            wr(("dO", so), ("dO", t))
+            arrive(f"do_full{so}", uo, 1)
             yield None
 
     def mma(kind, t):
@@ -110,55 +127,59 @@ def run(T, own_dq, new_order, seed, mutation=None, prod_prob=1.0):
     def commit(b, k):
         pipe_q.append(("commit", b, k))
 
+    def wait_q(t):  # the issuer's own check of Q(t) (none where it is vouched for)
+        if not vouch:
+            yield ("wait", f"q_full{t % nq}", t // nq)
+
     def issuer():
         yield ("wait", "kv_full", 0)
         yield ("wait", "q_full0", 0)
         mma("S", 0); commit("s_full", 0)
         for t in range(T):
-            st = t & 1
-            if mutation != "dP-skips-dO-wait":
-                yield ("wait", "do_full", t)
+            st = t % nq
+            if mutation != "dP-skips-dO-wait" and (not vouch or t == 0):
+                yield ("wait", f"do_full{t % ndo}", t // ndo)
             if not own_dq and t > 0 and mutation != "dP-skips-dQ-drain":
                 yield ("wait", "dq_empty", t - 1)
             mma("dP", t); commit("dp_full", t)
             yield ("wait", "p_ready", t)
             if mutation == "S-before-dV" and t + 1 < T:
-                yield ("wait", f"q_full{(t + 1) & 1}", (t + 1) >> 1)
+                yield from wait_q(t + 1)
                 mma("S", t + 1); commit("s_full", t + 1)
-            mma("dV", t); commit("do_empty", t)
+            mma("dV", t); commit(f"do_empty{t % ndo}", t // ndo)
             if new_order and mutation != "S-before-dV" and t + 1 < T:
-                yield ("wait", f"q_full{(t + 1) & 1}", (t + 1) >> 1)
+                yield from wait_q(t + 1)
                 mma("S", t + 1); commit("s_full", t + 1)
             yield ("wait", "ds_ready", t)
-            mma("dK", t); commit(f"q_empty{st}", t >> 1)
+            mma("dK", t); commit(f"q_empty{st}", t // nq)
             next_s_first = (not new_order) and own_dq   # main: d = 64 puts S^T(t+1) before dQ
             if next_s_first and t + 1 < T:
-                yield ("wait", f"q_full{(t + 1) & 1}", (t + 1) >> 1)
+                yield from wait_q(t + 1)
                 mma("S", t + 1); commit("s_full", t + 1)
-            if own_dq and t > 0:
+            if own_dq and t > 0 and not vouch:
                 yield ("wait", "dq_empty", t - 1)
             mma("dQ", t); commit("dq_full", t)
             if (not new_order) and (not next_s_first) and t + 1 < T:
-                yield ("wait", f"q_full{(t + 1) & 1}", (t + 1) >> 1)
+                yield from wait_q(t + 1)
                 mma("S", t + 1); commit("s_full", t + 1)
             yield None
         commit("acc_done", 0)
 
     def exec_mma(kind, t):
         if kind == "S":
-            rd(("Q", t & 1), ("Q", t)); rd("K", "K")
+            rd(("Q", t % nq), ("Q", t)); rd("K", "K")
             for w in W:
                 wr(A(w, "lo"), ("S", t)); wr(A(w, "hi"), ("S", t))
         elif kind == "dP":
-            rd("dO", ("dO", t))
+            rd(("dO", t % ndo), ("dO", t))
             for w in W:
                 wr(B(w, "lo"), ("dP", t)); wr(B(w, "hi"), ("dP", t))
         elif kind == "dV":
-            rd("dO", ("dO", t))
+            rd(("dO", t % ndo), ("dO", t))
             for w in W:
                 rd(A(w, "lo"), ("P", t))
         elif kind == "dK":
-            rd(("Q", t & 1), ("Q", t))
+            rd(("Q", t % nq), ("Q", t))
             for w in W:
                 rd(ds_reg(w), ("dS", t))
         elif kind == "dQ":
@@ -169,12 +190,14 @@ def run(T, own_dq, new_order, seed, mutation=None, prod_prob=1.0):
 
     def ew(w):
         for t in range(T):
-            st, u = t & 1, t >> 1
+            st, u = t % nq, t // nq
             yield ("wait", f"q_full{st}", u)
             yield ("wait", "s_full", t)
             rd(A(w, "lo"), ("S", t)); wr(A(w, "lo"), ("P_half", t)); yield None
             rd(A(w, "hi"), ("S", t)); wr(A(w, "lo"), ("P", t))
             rd(("Q", st), ("Q", t))  # L slice
+            if vouch and w == 0 and t + 1 < T and mutation != "vouch-skips-Q-check":
+                yield ("wait", f"q_full{(t + 1) % nq}", (t + 1) // nq)  # vouches for S^T(t+1)
             arrive("p_ready", t, 32)
             if mutation != "dS-without-dP-wait":
                 yield ("wait", "dp_full", t)
@@ -183,17 +206,27 @@ def run(T, own_dq, new_order, seed, mutation=None, prod_prob=1.0):
             yield None
             rd(B(w, "hi"), ("dP", t))
             wr(("smem_dS", w), ("dS", t)); wr(ds_reg(w), ("dS", t))
+            if vouch and w == 0 and t + 1 < T and mutation != "vouch-skips-dO-check":
+                yield ("wait", f"do_full{(t + 1) % ndo}", (t + 1) // ndo)  # vouches for dP^T(t+1)
             arrive("ds_ready", t, 32)
             yield None
         yield ("wait", "acc_done", 0)
 
     def dqw(q):
+        if vouch:
+            arrive("ds_ready", 0, 32)  # nothing to drain before dQ(0)
         for t in range(T):
             yield ("wait", "dq_full", t)
+            if vouch and mutation == "vouch-dQ-arrives-before-drain" and t + 1 < T:
+                arrive("ds_ready", t + 1, 32)
+                yield None
             for wg in (0, 1):
                 w = wg * 4 + q
                 rd(DQ(w, "lo"), ("dQ", t)); rd(DQ(w, "hi"), ("dQ", t))
-            arrive("dq_empty", t, 32)
+            if not vouch:
+                arrive("dq_empty", t, 32)
+            elif t + 1 < T and mutation != "vouch-dQ-arrives-before-drain":
+                arrive("ds_ready", t + 1, 32)  # vouches for dQ(t+1)'s columns
             yield None
 
     procs = {"prod": producer(), "mma": issuer()}
@@ -250,6 +283,30 @@ def test_protocol_is_free_of_deadlock_aliasing_and_hazards(order, d):
     for T in (1, 2, 3, 4, 5, 7):
         for seed in range(60):
             run(T, own_dq=(d == 64), new_order=ORDERS[order], seed=seed, prod_prob=0.15 if seed % 3 == 0 else 1.0)
+
+
+def test_vouched_protocol_at_d64_is_free_of_deadlock_aliasing_and_hazards():
+    for T in (1, 2, 3, 4, 5, 6, 7, 9):
+        for seed in range(80):
+            run(T, own_dq=True, new_order=True, seed=seed, prod_prob=(0.1, 0.4, 1.0)[seed % 3], vouch=True)
+
+
+@pytest.mark.parametrize("mutation", [
+    "vouch-skips-Q-check",            # S^T(t+1) would read a Q tile that has not landed
+    "vouch-skips-dO-check",           # dP^T(t+1) would read a dO tile that has not landed
+    "vouch-dQ-arrives-before-drain",  # dQ(t+1) would overwrite dQ(t) before its drain
+    "dP-skips-dO-wait",               # dP^T(0) would read a dO tile that has not landed
+])
+def test_planted_mistakes_in_the_vouched_protocol_are_caught(mutation):
+    failures = 0
+    for T in (2, 3, 4, 5):
+        for seed in range(60):
+            try:
+                run(T, own_dq=True, new_order=True, seed=seed, mutation=mutation, prod_prob=0.1 if seed & 1 else 0.5,
+                    vouch=True)
+            except Err:
+                failures += 1
+    assert failures > 0, f"{mutation} went unnoticed"
 
 
 @pytest.mark.parametrize("mutation, order, d", [

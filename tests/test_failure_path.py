@@ -7,6 +7,9 @@ a producer withhold one load -- a barrier that nothing completes:
 * backward: no dO tile is loaded, so dP^T and dV never start while S^T, the
   P phase and the other roles run up to their waits.
 
+Both head sizes run it: at d = 64 the backward also takes the path where
+other roles vouch for the MMA thread's checks.
+
 Every wait then expires (about 2 s) or sees the CTA's abort flag, the CTA
 skips its remaining work, lets copies and MMAs already in flight land, frees
 its tensor memory and records FA_ERR_TIMEOUT in the device status word.  The
@@ -34,7 +37,7 @@ CHILD = textwrap.dedent("""
     lib = fa.load(fa_build.build_test_hooks())
     lib.fa_test_set_withhold.argtypes = [ctypes.c_int]
     lib.fa_test_set_withhold.restype = None
-    Q, K, V, dO = make_custom(1, 4, 2, 300, 333, 128, True, seed=5)
+    Q, K, V, dO = make_custom(1, 4, 2, 300, 333, {d}, True, seed=5)
     dev = torch.device("cuda")
     Qd, Kd, Vd, dOd = Q.to(dev), K.to(dev), V.to(dev), dO.to(dev)
 
@@ -66,11 +69,12 @@ CHILD = textwrap.dedent("""
 
 
 @pytest.mark.gpu
-def test_withheld_loads_time_out_and_context_survives():
+@pytest.mark.parametrize("d", [64, 128])
+def test_withheld_loads_time_out_and_context_survives(d):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT)], cwd=ROOT, capture_output=True, text=True,
-                       timeout=600)
+    r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT, d=d)], cwd=ROOT, capture_output=True,
+                       text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
     line = [ln for ln in r.stdout.splitlines() if ln.startswith("STATUS")][-1]
     _, s_fwd, s_fwd_ok, s_bwd, s_bwd_ok, t_fwd, t_bwd = line.split()

@@ -75,24 +75,33 @@ static_assert(kRegsLow % 8 == 0 && kRegsHigh % 8 == 0 && kRegsHigh <= 256, "setm
 // HD: head size of Q and K; HDV: head size of V, O and dO.
 template <int HD, int HDV>
 struct BwdCfg {
+  // d = dv = 64 leaves shared memory for deeper Q and dO rings.  Loads then
+  // land a tile earlier, and other roles can vouch for three of the MMA
+  // thread's five checks per tile (see the kernel): one elementwise thread
+  // checks Q(t+1) before it releases P(t) and dO(t+1) before it releases
+  // dS(t), and the dQ warps arrive on ds_ready(t+1) once dQ(t) is drained.
+  static constexpr bool VOUCH = HD == 64 && HDV == 64;
+  static constexpr int NQ = VOUCH ? 3 : 2;   // Q tiles (with their L and D slices) in flight
+  static constexpr int NDO = VOUCH ? 2 : 1;  // dO tiles in flight
   static constexpr int QK_TILE = 128 * HD * 2;   // one Q or K tile (bf16)
   static constexpr int VO_TILE = 128 * HDV * 2;  // one V or dO tile (bf16)
   static constexpr int DS_BYTES = BN * BM * 2;
   static constexpr int STG_SLOT = 32 * 32 * 4;  // one warp's 32 rows x 32 fp32 columns
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + QK_TILE;
-  static constexpr int OFF_Q = OFF_V + VO_TILE;       // [2]
-  static constexpr int OFF_DO = OFF_Q + 2 * QK_TILE;  // [1]
-  static constexpr int OFF_DS = OFF_DO + VO_TILE;
+  static constexpr int OFF_Q = OFF_V + VO_TILE;         // [NQ]
+  static constexpr int OFF_DO = OFF_Q + NQ * QK_TILE;   // [NDO]
+  static constexpr int OFF_DS = OFF_DO + NDO * VO_TILE;
   // Epilogue staging of dV and dK over the Q ring and the dO buffer (idle by then).
   static constexpr int OFF_DV_STAGE = OFF_Q;
   static constexpr int OFF_DK_STAGE = OFF_Q + (QK_TILE > VO_TILE ? QK_TILE : VO_TILE);
   static_assert(OFF_DK_STAGE + QK_TILE <= OFF_DS, "dV / dK staging fits in the Q ring and dO buffer");
   static constexpr int OFF_STG = OFF_DS + DS_BYTES;       // [4 warps][2] dQ staging slots
-  static constexpr int OFF_LSE = OFF_STG + 8 * STG_SLOT;  // [2][128] fp32
-  static constexpr int OFF_DELTA = OFF_LSE + 2 * 512;  // [2][128] fp32
-  static constexpr int OFF_BAR = OFF_DELTA + 2 * 512;
+  static constexpr int OFF_LSE = OFF_STG + 8 * STG_SLOT;  // [NQ][128] fp32
+  static constexpr int OFF_DELTA = OFF_LSE + NQ * 512;   // [NQ][128] fp32
+  static constexpr int OFF_BAR = OFF_DELTA + NQ * 512;
   static constexpr int NBAR = 24;
+  static_assert(1 + 2 * NQ + 2 * NDO + 8 <= NBAR, "barrier slots");
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -195,20 +204,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tmAcc, const BwdParams p) {
   using C = BwdCfg<HD, HDV>;
   extern __shared__ __align__(1024) uint8_t smem[];
+  constexpr int NQ = C::NQ, NDO = C::NDO;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars + 0;
-  uint64_t* q_full = bars + 1;   // [2]
-  uint64_t* q_empty = bars + 3;  // [2]
-  uint64_t* do_full = bars + 5;
-  uint64_t* do_empty = bars + 6;
-  uint64_t* s_full = bars + 7;
-  uint64_t* dp_full = bars + 8;
-  uint64_t* p_ready = bars + 9;
-  uint64_t* ds_ready = bars + 10;
-  uint64_t* dq_full = bars + 12;
-  uint64_t* dq_empty = bars + 13;
-  uint64_t* acc_done = bars + 14;
-  uint64_t* drain = bars + 15;
+  uint64_t* q_full = bars + 1;         // [NQ]
+  uint64_t* q_empty = q_full + NQ;     // [NQ]
+  uint64_t* do_full = q_empty + NQ;    // [NDO]
+  uint64_t* do_empty = do_full + NDO;  // [NDO]
+  uint64_t* s_full = do_empty + NDO;
+  uint64_t* dp_full = s_full + 1;
+  uint64_t* p_ready = s_full + 2;
+  uint64_t* ds_ready = s_full + 3;
+  uint64_t* dq_full = s_full + 4;
+  uint64_t* dq_empty = s_full + 5;
+  uint64_t* acc_done = s_full + 6;
+  uint64_t* drain = s_full + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile unsigned int* split_seen = reinterpret_cast<volatile unsigned int*>(tmem_slot + 2);  // halves counted before
@@ -258,16 +268,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = (smem_u32(smem) & 1023u) ? 1 : 0;
     mbar_init(kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NQ; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
     }
-    mbar_init(do_full, 1);
-    mbar_init(do_empty, 1);
+    for (int s = 0; s < NDO; ++s) {
+      mbar_init(&do_full[s], 1);
+      mbar_init(&do_empty[s], 1);
+    }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 256);
-    mbar_init(ds_ready, 256);
+    // with VOUCH the dQ warps arrive too, once the previous dQ tile is drained
+    mbar_init(ds_ready, C::VOUCH ? 384 : 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(acc_done, 1);
@@ -307,9 +320,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int cb = 0; cb < HD / 64; ++cb) tma_load_3d(smem + C::OFF_K + cb * BN * 128, &tmK, kv_full, cb * 64, k0, bkv);
 #pragma unroll
       for (int cb = 0; cb < HDV / 64; ++cb) tma_load_3d(smem + C::OFF_V + cb * BN * 128, &tmV, kv_full, cb * 64, k0, bkv);
-      int last_q[2] = {-1, -1}, last_do = -1;
+      int last_q[NQ], last_do[NDO];
+      for (int s = 0; s < NQ; ++s) last_q[s] = -1;
+      for (int s = 0; s < NDO; ++s) last_do[s] = -1;
       for (int t = 0; t < T; ++t) {
-        const int st = t & 1, u = t >> 1;
+        const int st = t % NQ, u = t / NQ;
         const int g = (t0 + t) / n_m, m = m_begin + ((t0 + t) - g * n_m);
         const int bh = b * p.Hq + hk * p.G + g;
         if (!mbar_wait(&q_empty[st], (u & 1) ^ 1, abort_flag)) break;
@@ -321,24 +336,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(smem + C::OFF_LSE + st * 512, p.lse2 + row0, 512, &q_full[st]);
         bulk_load(smem + C::OFF_DELTA + st * 512, p.delta + row0, 512, &q_full[st]);
         last_q[st] = u;
-        // dO has one buffer, refilled only once dV_{t-1} is done: pull it into
-        // L2 now so that its load later does not stall the dP MMA.
+        // A dO slot is refilled only once dV of the tile before is done: pull
+        // the tile into L2 now so that its load later does not stall the dP MMA.
 #pragma unroll
         for (int cb = 0; cb < HDV / 64; ++cb) tma_prefetch_l2_3d(&tmdO, cb * 64, m * BM, bh);
-        if (!mbar_wait(do_empty, (t & 1) ^ 1, abort_flag)) break;
+        const int so = t % NDO, uo = t / NDO;
+        if (!mbar_wait(&do_empty[so], (uo & 1) ^ 1, abort_flag)) break;
 #ifdef FA_TEST_HOOKS
         if (p.test_withhold_do) continue;
 #endif
-        mbar_arrive_expect_tx(do_full, C::VO_TILE);
+        mbar_arrive_expect_tx(&do_full[so], C::VO_TILE);
 #pragma unroll
         for (int cb = 0; cb < HDV / 64; ++cb)
-          tma_load_3d(smem + C::OFF_DO + cb * BM * 128, &tmdO, do_full, cb * 64, m * BM, bh);
-        last_do = t;
+          tma_load_3d(smem + C::OFF_DO + so * C::VO_TILE + cb * BM * 128, &tmdO, &do_full[so], cb * 64, m * BM, bh);
+        last_do[so] = uo;
       }
       mbar_wait_bounded(kv_full, 0);
-      for (int st = 0; st < 2; ++st)
-        if (last_q[st] >= 0) mbar_wait_bounded(&q_full[st], last_q[st] & 1);
-      if (last_do >= 0) mbar_wait_bounded(do_full, last_do & 1);
+      for (int s = 0; s < NQ; ++s)
+        if (last_q[s] >= 0) mbar_wait_bounded(&q_full[s], last_q[s] & 1);
+      for (int s = 0; s < NDO; ++s)
+        if (last_do[s] >= 0) mbar_wait_bounded(&do_full[s], last_do[s] & 1);
     } else if (warp == 1 && lane == 0 && run) {
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t id_sdp = idesc_bf16(BN, BM, 0, 0);  // S^T, dP^T: M = keys, N = queries
@@ -347,10 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_q = idesc_bf16(BM, HD, 1, 1);    // dQ: M = queries (A MN-major), N = d
       const uint32_t k_base = smem_u32(smem + C::OFF_K), v_base = smem_u32(smem + C::OFF_V);
       const uint32_t ds_base = smem_u32(smem + C::OFF_DS);
-      const uint32_t do_base = smem_u32(smem + C::OFF_DO);
       // S^T(t) = K Q_t^T into T_S
       auto mma_s = [&](int t) {
-        const uint32_t q_base = smem_u32(smem + C::OFF_Q + (t & 1) * C::QK_TILE);
+        const uint32_t q_base = smem_u32(smem + C::OFF_Q + (t % NQ) * C::QK_TILE);
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k)
           mma_ss(T_S, desc_kmajor(k_base + (k >> 2) * (BN * 128) + (k & 3) * 32),
@@ -363,16 +379,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // have been read by then.  With S^T(t+1) right behind dV(t), the
       // elementwise warps go from tile t's dS phase straight to tile t+1's P
       // phase while dK(t), dQ(t) and dP^T(t+1) run.
+      // With VOUCH the thread checks only p_ready(t) and ds_ready(t) per tile
+      // (and dO(0)): those barriers also stand for Q(t+1) (before S^T(t+1)),
+      // for dO(t+1) and for the drain of dQ(t) (before dQ(t+1) and dP^T(t+1)),
+      // so dK(t), dQ(t) and dP^T(t+1) go out as one run of MMAs.
       bool ok = mbar_wait(kv_full, 0, abort_flag) && mbar_wait(&q_full[0], 0, abort_flag);
       if (ok) {
         tc_fence_after();
         mma_s(0);
       }
       for (int t = 0; ok && t < T; ++t) {
-        const int st = t & 1;
+        const int st = t % NQ, so = t % NDO;
         const uint32_t q_base = smem_u32(smem + C::OFF_Q + st * C::QK_TILE);
+        const uint32_t do_base = smem_u32(smem + C::OFF_DO + so * C::VO_TILE);
+        if ((!C::VOUCH || t == 0) && !mbar_wait(&do_full[so], (t / NDO) & 1, abort_flag)) { ok = false; break; }
         // dP^T shares its TMEM columns with dQ (d = 128): the previous tile's dQ must be drained
-        if (!mbar_wait(do_full, t & 1, abort_flag)) { ok = false; break; }
         if (!kOwnDQ && t > 0 && !mbar_wait(dq_empty, (t - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
@@ -389,10 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < BM / 16; ++k)
           mma_ts(T_DV, T_S + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(do_base + k * 2048, BM * 128), id_dv,
                  (t > 0 || k > 0) ? 1u : 0u);
-        mma_commit(do_empty);
+        mma_commit(&do_empty[so]);
         if (t + 1 < T) {
-          if (!mbar_wait(&q_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
+          if (!C::VOUCH) {
+            if (!mbar_wait(&q_full[(t + 1) % NQ], ((t + 1) / NQ) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+          }
           mma_s(t + 1);
         }
         // dS^T lives in TMEM as packed bf16 over dP^T, in the same column
@@ -408,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(T_DK, T_DP + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(q_base + k * 2048, BM * 128), id_dk,
                  (t > 0 || k > 0) ? 1u : 0u);
         mma_commit(&q_empty[st]);
-        if (kOwnDQ && t > 0) {  // dQ(t-1) drained from its columns
+        if (kOwnDQ && !C::VOUCH && t > 0) {  // dQ(t-1) drained from its columns
           if (!mbar_wait(dq_empty, (t - 1) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
         }
@@ -432,8 +455,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool key_valid = key < p.Tk;
     const float sl2 = p.scale_log2;
     bool ok = run;
+    // With VOUCH one thread checks the next tile's Q before releasing P and
+    // its dO before releasing dS, standing in for the MMA thread's checks.
+    const bool voucher = C::VOUCH && warp == 4 && lane == 0;
     for (int t = 0; ok && t < T; ++t) {
-      const int st = t & 1, u = t >> 1;
+      const int st = t % NQ, u = t / NQ;
       const int g = (t0 + t) / n_m, m = m_begin + ((t0 + t) - g * n_m);
       const int q0 = m * BM;
       const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE + st * 512);
@@ -488,7 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
+      if (voucher && t + 1 < T && !mbar_wait(&q_full[(t + 1) % NQ], ((t + 1) / NQ) & 1, abort_flag)) ok = false;
       mbar_arrive(p_ready);
+      if (C::VOUCH && !__all_sync(0xffffffffu, ok)) { ok = false; break; }  // the warp stops as one
       // ---- dS = P * (dP - D) -> shared memory (row = key, 128B-swizzled, query-contiguous)
       // dP^T is in TMEM.  The previous tile's dQ MMA, which reads dS from shared
       // memory, was issued before this tile's dP^T by the same thread, so the
@@ -526,7 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       fence_async_smem();
       tc_fence_before();
+      if (voucher && t + 1 < T && !mbar_wait(&do_full[(t + 1) % NDO], ((t + 1) / NDO) & 1, abort_flag)) ok = false;
       mbar_arrive(ds_ready);
+      if (C::VOUCH && !__all_sync(0xffffffffu, ok)) { ok = false; break; }
     }
     // ---- epilogue: dV, dK * scale -> bf16 -> shared (the Q ring, idle now) -> TMA store
     if (ok && T > 0) {
@@ -590,6 +620,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* wslot = smem + C::OFF_STG + quad * (2 * C::STG_SLOT);
     constexpr int NCH = HD / 32;  // 32-column chunks per tile
     bool ok = run;
+    // With VOUCH the drain is announced on ds_ready(t+1) (which the MMA thread
+    // waits for before dQ(t+1) anyway); there is nothing to drain before dQ(0).
+    if (C::VOUCH && ok) mbar_arrive(ds_ready);
     for (int t = 0; ok && t < T; ++t) {
       const int g = (t0 + t) / n_m, m = m_begin + ((t0 + t) - g * n_m);
       const int bh = b * p.Hq + hk * p.G + g;
@@ -600,7 +633,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < NCH; ++c) tmem_ld32(T_DQ + lane_base + c * 32, v[c]);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(dq_empty);  // all of dQ_t is out of TMEM: it may take dP_{t+1} (or dQ_{t+1})
+      // all of dQ_t is out of TMEM: it may take dP_{t+1} (or dQ_{t+1})
+      if (!C::VOUCH)
+        mbar_arrive(dq_empty);
+      else if (t + 1 < T)
+        mbar_arrive(ds_ready);
 #pragma unroll
       for (int c = 0; c < NCH; c += 2) {
         if (leader) bulk_wait_read0();  // both slots read by the previous reduce-adds
