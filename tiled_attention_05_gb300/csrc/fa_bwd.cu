@@ -11,8 +11,12 @@
 // Three kernels:
 //   fa_bwd_pre   D = rowsum(dO * O), L in log2 units (+inf on padding rows so
 //                that their probabilities vanish), zero the fp32 dQ
-//                accumulator.  HBM-bound, one warp per row.
-//   fa_bwd_main  one CTA per (batch, kv head, 128-key tile): K and V stay in
+//                accumulator and the split items' counters.  HBM-bound, a row
+//                per group of dv / 8 lanes.
+//   fa_bwd_main  one CTA per (batch, kv head, 128-key tile) -- without a causal
+//                mask, a short last round of tiles runs as two CTAs per tile,
+//                each over half of its query tiles, whose fp32 dK / dV meet in
+//                the workspace -- K and V stay in
 //                shared memory; the CTA walks the G query heads of its group
 //                and the 128-row query tiles that can see its keys (causal:
 //                from the diagonal on; with a sliding window of W keys, up to
@@ -23,7 +27,8 @@
 //
 // fa_bwd_main roles (512 threads, four warpgroups):
 //   warp 0      TMA: K, V once; then Q_t (+ the tile's L and D slices by 1-D
-//               bulk copy) through a 2-deep ring and dO_t through one buffer.
+//               bulk copy) through a 2-deep ring and dO_t through one buffer
+//               (3-deep and 2 buffers at d = dv = 64).
 //   warp 1      tcgen05 issuer, per tile t:
 //                 dP^T = V dO_t^T       -> TMEM [128,256)
 //                 dV  += P^T dO_t       A = P^T from TMEM (bf16, written over S^T)
@@ -33,7 +38,10 @@
 //                                        columns after dK; A = the dS bytes in
 //                                        shared memory read MN-major; B = K read MN-major
 //               relying on in-order MMA execution, not on waits, wherever a
-//               later MMA overwrites columns an earlier one reads.
+//               later MMA overwrites columns an earlier one reads.  At
+//               d = dv = 64 it checks only P and dS per tile: one elementwise
+//               thread and the dQ warps vouch for Q_{t+1}, dO_{t+1} and the
+//               drained dQ columns.
 //   warps 4..11 two elementwise warpgroups (thread = key row = TMEM lane; group
 //               w owns query columns [64w, 64w+64)): P = exp2(S*scale*log2e - L2)
 //               with masks -> TMEM; dS = P * (dP - D) -> shared memory (for the
