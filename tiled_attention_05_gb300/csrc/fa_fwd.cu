@@ -12,6 +12,9 @@
 // the CTA loads for it; each CTA walks its items (heaviest causal rows first,
 // in a snake order over the CTAs so that their totals even out) and starts
 // the next item's loads and first MMAs while the current one finishes.
+// Without a causal mask (items of equal work) a last round with at most half
+// as many items as SMs is run as single-tile items (tile B left empty) on
+// twice as many SMs.
 //   warp 0       TMA producer: Q_A, Q_B per item (each as soon as the last
 //                S of the previous item's tile has read its buffer), then the
 //                item's K_j / V_j through NS-deep rings that run on across items.
