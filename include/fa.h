@@ -88,18 +88,27 @@ typedef struct {
 FA_API fa_status fa_forward(const fa_dims* dims, const void* Q, const void* K, const void* V, void* O, float* L,
                      void* stream);
 
-/* Size in bytes of the scratch buffer fa_backward needs: an fp32 dQ
- * accumulator [B, Hq, ceil(Tq/128)*128, d] plus two fp32 row vectors
- * (D and log2-scaled L) of B*Hq*ceil(Tq/128)*128 entries, plus alignment;
- * without a causal mask also room for the partial dK / dV
- * of up to min(B*Hkv*ceil(Tk/128), 128) key tiles whose work is split in two
- * (fp32, 2 x 128 x (d + dv) each) and a 4-byte counter per such tile. */
+/* Size in bytes of the scratch buffer for fa_backward's fastest schedule:
+ * an fp32 dQ accumulator [B, Hq, ceil(Tq/128)*128, d] plus two fp32 row
+ * vectors (D and log2-scaled L) of B*Hq*ceil(Tq/128)*128 entries, plus
+ * alignment; without a causal mask also room for the partial dK / dV of up
+ * to min(B*Hkv*ceil(Tk/128), 128) key tiles whose work may be split in two
+ * (fp32, 2 x 128 x (d + dv) each) and a 4-byte counter per such tile.
+ * Returns 0 for invalid dims. */
 FA_API size_t fa_backward_workspace_bytes(const fa_dims* dims);
+
+/* The least workspace fa_backward accepts: the dQ accumulator and the two
+ * row vectors alone.  With less than fa_backward_workspace_bytes(dims) the
+ * backward runs every key tile as one work item (same results, a slower
+ * last round without a causal mask).  Equal to fa_backward_workspace_bytes
+ * with a causal mask.  Returns 0 for invalid dims. */
+FA_API size_t fa_backward_workspace_min_bytes(const fa_dims* dims);
 
 /* Backward pass from O, L of fa_forward (same dims) and the upstream gradient
  * dO.  Writes dQ, dK, dV.  `workspace` must hold at least
- * fa_backward_workspace_bytes(dims) bytes, 256-byte aligned; its contents on
- * entry are ignored. */
+ * fa_backward_workspace_min_bytes(dims) bytes (fa_backward_workspace_bytes
+ * for the fastest schedule), 256-byte aligned; its contents on entry are
+ * ignored. */
 FA_API fa_status fa_backward(const fa_dims* dims, const void* Q, const void* K, const void* V, const void* O,
                       const void* dO, const float* L, void* dQ, void* dK, void* dV, void* workspace,
                       size_t workspace_bytes, void* stream);
@@ -123,9 +132,10 @@ FA_API fa_status fa_backward_stages(const fa_dims* dims, const void* Q, const vo
  * FA_NOALLOC_SCRATCH_BYTES that the library keeps in device memory on every
  * GPU that loads it, for the life of the process.  This entry point has no
  * counterpart on the pages; it is an interface convenience.
- *  - A problem whose fa_backward_workspace_bytes exceeds
+ *  - A problem whose fa_backward_workspace_min_bytes exceeds
  *    FA_NOALLOC_SCRATCH_BYTES is rejected with FA_ERR_SCRATCH_TOO_SMALL
- *    before anything is enqueued (use fa_backward for it).
+ *    before anything is enqueued (use fa_backward for it); one that fits
+ *    the minimum but not fa_backward_workspace_bytes runs unsplit.
  *  - Nothing is allocated or freed.  The first call on each device looks up
  *    the array's device address with that device current and keeps it for
  *    the life of the process; make that first call before any stream capture

@@ -88,7 +88,8 @@ def test_zero_sized_problems_are_noops():
 def test_backward_workspace_validation():
     lib = fa.load()
     d = dims()
-    need = fa.fa_backward_workspace_bytes(d)
+    need = fa.fa_backward_workspace_min_bytes(d)
+    assert 0 < need < fa.fa_backward_workspace_bytes(d)  # non-causal: the split area is optional
     p = [0x1000 * (i + 1) for i in range(9)]
     # too small, misaligned, null workspace
     for ws, nbytes in ((0x100000, need - 1), (0x100010, need), (0, need)):
@@ -107,7 +108,9 @@ def test_workspace_size_formula():
         cap = min(B * 1 * ((Tk + 127) // 128), 128) if not causal else 0
         want = up(base + cap * 2 * 128 * (2 * dd) * 4) + cap * 4
         assert fa.fa_backward_workspace_bytes(d) == up(want)
+        assert fa.fa_backward_workspace_min_bytes(d) == base
     assert fa.fa_backward_workspace_bytes(dims(Hq=3, Hkv=2)) == 0
+    assert fa.fa_backward_workspace_min_bytes(dims(Hq=3, Hkv=2)) == 0
 
 
 def test_binding_constants_match_the_header():

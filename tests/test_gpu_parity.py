@@ -106,6 +106,28 @@ def test_split_work_items(fa, shape):
     assert_close("dV", got["dV"], dV)
 
 
+@pytest.mark.parametrize("shape", SPLIT[:2] + SPLIT[3:], ids=lambda s: "x".join(map(str, s)))
+def test_backward_with_the_least_workspace(fa, shape):
+    """A workspace of fa_backward_workspace_min_bytes (no room for the split
+    area) runs every key tile as one work item: same results."""
+    B, Hq, Hkv, Tq, Tk, d = shape
+    Q, K, V, dO = make_custom(B, Hq, Hkv, Tq, Tk, d, False, seed=sum(shape) + 6)
+    dev = torch.device("cuda")
+    Qd, Kd, Vd, dOd = (t.to(dev) for t in (Q, K, V, dO))
+    O, L = fa.fa_forward(Qd, Kd, Vd, False)
+    dims = fa.make_dims(B, Hq, Hkv, Tq, Tk, d, d, False, None)
+    least = fa.fa_backward_workspace_min_bytes(dims)
+    assert least < fa.fa_backward_workspace_bytes(dims)
+    ws = torch.empty(least, dtype=torch.uint8, device=dev)
+    dQ, dK, dV = fa.fa_backward(Qd, Kd, Vd, O, dOd, L, False, workspace=ws)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    dQr, dKr, dVr, _ = oracle.backward(Q, K, V, dO, False)
+    assert_close("dQ", dQ.cpu(), dQr)
+    assert_close("dK", dK.cpu(), dKr)
+    assert_close("dV", dV.cpu(), dVr)
+
+
 @pytest.mark.parametrize("Tq", [32, 300])
 def test_appended_queries_over_long_prefix(fa, Tq):
     """Queries appended after an ~8000-token prefix (Tk = 8000 + 32, 32 query / 8

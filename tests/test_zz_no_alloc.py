@@ -51,7 +51,7 @@ def test_noalloc_matches_backward_twice(fa, first, second):
         B, Hq, Hkv, Tq, Tk, d, causal = shape
         Q, K, V, dO = (t.to(dev) for t in make_custom(B, Hq, Hkv, Tq, Tk, d, causal, seed=Tq + Tk))
         dims = fa.make_dims(B, Hq, Hkv, Tq, Tk, d, d, causal, None)
-        assert fa.fa_backward_workspace_bytes(dims) <= fa.FA_NOALLOC_SCRATCH_BYTES
+        assert fa.fa_backward_workspace_min_bytes(dims) <= fa.FA_NOALLOC_SCRATCH_BYTES
         O, L = fa.fa_forward(Q, K, V, causal)
         ref = fa.fa_backward(Q, K, V, O, dO, L, causal)
         got = _noalloc_via_abi(fa, dims, Q, K, V, O, dO, L)
@@ -64,7 +64,7 @@ def test_noalloc_matches_backward_twice(fa, first, second):
 def test_noalloc_rejects_problems_beyond_its_scratch(fa):
     # 2 x 32 heads x 8192 rows needs ~272 MB of workspace: refused before anything is enqueued.
     dims = fa.make_dims(2, 32, 8, 8192, 8192, 128, 128, True, None)
-    assert fa.fa_backward_workspace_bytes(dims) > fa.FA_NOALLOC_SCRATCH_BYTES
+    assert fa.fa_backward_workspace_min_bytes(dims) > fa.FA_NOALLOC_SCRATCH_BYTES
     p = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(9)]
     code = fa.load().fa_backward_noalloc(ctypes.byref(dims), *p, None)
     assert code == fa.FA_ERR_SCRATCH_TOO_SMALL

@@ -7,7 +7,8 @@ library cannot be loaded, every entry point raises.
 Entry points mirror the C ABI:
     fa_forward(Q, K, V, causal, scale=None, window=0)            -> (O, L)
     fa_backward(Q, K, V, O, dO, L, causal, scale=None, window=0)  -> (dQ, dK, dV)
-    fa_backward_workspace_bytes(...), fa_status_string(code), fa_last_device_status()
+    fa_backward_workspace_bytes(...), fa_backward_workspace_min_bytes(...), fa_status_string(code),
+    fa_last_device_status()
 plus ``FlashAttention`` (a torch.autograd.Function that keeps only Q, K, V, O
 and L for the backward pass) and ``attention`` (its functional form).
 
@@ -26,7 +27,8 @@ from . import build as _build
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 
 EXPORTED_SYMBOLS = ("fa_forward", "fa_backward", "fa_backward_stages", "fa_backward_workspace_bytes",
-                    "fa_backward_noalloc", "fa_status_string", "fa_last_device_status", "fa_last_launch_count")
+                    "fa_backward_workspace_min_bytes", "fa_backward_noalloc", "fa_status_string",
+                    "fa_last_device_status", "fa_last_launch_count")
 FA_ERR_SCRATCH_TOO_SMALL = 5
 FA_NOALLOC_SCRATCH_BYTES = 32 << 20
 FA_BWD_PRE, FA_BWD_MAIN, FA_BWD_CAST, FA_BWD_ALL = 1, 2, 4, 7
@@ -73,6 +75,8 @@ def load(path: str | None = None):
             lib.fa_backward_noalloc.restype = ctypes.c_int
             lib.fa_backward_workspace_bytes.argtypes = [dp]
             lib.fa_backward_workspace_bytes.restype = ctypes.c_size_t
+            lib.fa_backward_workspace_min_bytes.argtypes = [dp]
+            lib.fa_backward_workspace_min_bytes.restype = ctypes.c_size_t
             lib.fa_status_string.argtypes = [ctypes.c_int]
             lib.fa_status_string.restype = ctypes.c_char_p
             lib.fa_last_device_status.argtypes = [vp]
@@ -138,7 +142,13 @@ def _raise(code: int, where: str):
 
 
 def fa_backward_workspace_bytes(dims: FaDims) -> int:
+    """Workspace for the backward's fastest schedule (what fa_backward allocates)."""
     return int(load().fa_backward_workspace_bytes(ctypes.byref(dims)))
+
+
+def fa_backward_workspace_min_bytes(dims: FaDims) -> int:
+    """The least workspace fa_backward accepts (then no work item is split)."""
+    return int(load().fa_backward_workspace_min_bytes(ctypes.byref(dims)))
 
 
 def fa_forward(Q, K, V, causal: bool, scale: float | None = None, O=None, L=None, stream=None, window: int = 0):

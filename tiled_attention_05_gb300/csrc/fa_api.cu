@@ -169,6 +169,12 @@ size_t fa_backward_workspace_bytes(const fa_dims* dims) {
   return fa::backward_workspace_layout(pr).total;
 }
 
+size_t fa_backward_workspace_min_bytes(const fa_dims* dims) {
+  fa::Problem pr;
+  if (check_dims(dims, &pr) != FA_OK) return 0;
+  return fa::backward_workspace_layout(pr).total_min;
+}
+
 fa_status fa_backward_stages(const fa_dims* dims, const void* Q, const void* K, const void* V, const void* O,
                              const void* dO, const float* L, void* dQ, void* dK, void* dV, void* workspace,
                              size_t workspace_bytes, int stages, void* stream) {
@@ -184,14 +190,14 @@ fa_status fa_backward_stages(const fa_dims* dims, const void* Q, const void* K, 
       (s = check_ptr(dK, nk)) || (s = check_ptr(dV, nkv)))
     return s;
   if ((nq == 0 && nk == 0) || stages == 0) return FA_OK;
-  const size_t need = fa::backward_workspace_layout(pr).total;
+  const size_t need = fa::backward_workspace_layout(pr).total_min;
   if (nq > 0 && nk > 0) {
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
       return FA_ERR_INVALID_ARG;
   }
   if (!fa::device_status_word()) return FA_ERR_CUDA;
   int launches = 0;
-  cudaError_t e = fa::launch_backward(pr, Q, K, V, O, dO, L, dQ, dK, dV, workspace, stages,
+  cudaError_t e = fa::launch_backward(pr, Q, K, V, O, dO, L, dQ, dK, dV, workspace, workspace_bytes, stages,
                                       static_cast<cudaStream_t>(stream), &launches);
   t_last_launches = launches;
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;

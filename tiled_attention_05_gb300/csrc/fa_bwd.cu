@@ -844,6 +844,7 @@ BwdWorkspace backward_workspace_layout(const Problem& p) {
   w.lse2 = up(w.dq_acc + rows * p.d * sizeof(float));
   w.delta = up(w.lse2 + rows * sizeof(float));
   w.part = up(w.delta + rows * sizeof(float));
+  w.total_min = w.part;
   // Items have equal work without a causal mask: then a short last round may
   // be split (up to kMaxSplitItems items).  (With a window the last key
   // tiles of each head are lighter, and splitting did not pay.)
@@ -870,7 +871,7 @@ int backward_split_items(const Problem& p, int split_cap) {
 
 cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, const void* V, const void* O,
                             const void* dO, const float* L, void* dQ, void* dK, void* dV, void* workspace,
-                            int stages, cudaStream_t stream, int* launches) {
+                            size_t workspace_bytes, int stages, cudaStream_t stream, int* launches) {
   const long long q_rows = (long long)pr.B * pr.Hq * pr.Tq;
   const long long k_rows = (long long)pr.B * pr.Hkv * pr.Tk;
   if (q_rows == 0 && k_rows == 0) return cudaSuccess;
@@ -892,6 +893,8 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
     return cudaGetLastError();
   }
   const BwdWorkspace w = backward_workspace_layout(pr);
+  // the split items' area is used only where the caller's workspace holds it
+  const int split_cap = workspace_bytes >= w.total ? w.split_cap : 0;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
   float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
@@ -906,7 +909,7 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
   auto pre = pr.d == 64 ? (pr.dv == 64 ? fa_bwd_pre<64, 64> : fa_bwd_pre<64, 128>)
                         : (pr.dv == 64 ? fa_bwd_pre<128, 64> : fa_bwd_pre<128, 128>);
   pre<<<grid_for(rows_pad, 8 * 2 * (32 / (pr.dv / 8))), 256, 0, stream>>>(static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), L,
-                                                 lse2, delta, dq_acc, split_counters, w.split_cap, rows_pad, pr.Tq,
+                                                 lse2, delta, dq_acc, split_counters, split_cap, rows_pad, pr.Tq,
                                                  pr.Tq_pad());
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -943,7 +946,7 @@ cudaError_t launch_backward(const Problem& pr, const void* Q, const void* K, con
   bp.scale = pr.scale;
   bp.scale_log2 = pr.scale * 1.4426950408889634f;
   bp.test_withhold_do = fa::test_withhold() == fa::kWithholdBwdDO;
-  bp.n_split = backward_split_items(pr, w.split_cap);
+  bp.n_split = backward_split_items(pr, split_cap);
   bp.n_whole = (int)((long long)pr.B * pr.Hkv * pr.kv_tiles()) - bp.n_split;
   bp.part = part;
   bp.split_counters = split_counters;

@@ -52,9 +52,10 @@ cudaError_t allow_dynamic_smem(const void* kernel, int bytes);
 // of kernels it enqueued to *launches.
 cudaError_t launch_forward(const Problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
                            cudaStream_t stream, int* launches);
+// `workspace_bytes` decides whether the split-item area fits (see BwdWorkspace).
 cudaError_t launch_backward(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                             const void* dO, const float* L, void* dQ, void* dK, void* dV, void* workspace,
-                            int stages, cudaStream_t stream, int* launches);
+                            size_t workspace_bytes, int stages, cudaStream_t stream, int* launches);
 
 // Groups per super-batch of the backward's grid order: the smallest divisor
 // S of n_groups with S * kv_tiles >= 1.5 * sms, searched up to four times the
@@ -74,9 +75,11 @@ constexpr int kMaxSplitItems = 128;
 
 // Workspace carve-up of fa_backward (byte offsets, 256-aligned).  `part` and
 // `counters` (the split items' partial dK / dV and their finish counters)
-// are empty when no item can be split (with a causal mask).
+// are empty when no item can be split (with a causal mask).  The backward
+// needs `total_min` bytes (up to `part`); it splits items only when the
+// workspace also holds the split area (`total`).
 struct BwdWorkspace {
-  size_t dq_acc, lse2, delta, part, counters, total;
+  size_t dq_acc, lse2, delta, part, counters, total_min, total;
   int split_cap;  // items the partial area has room for
 };
 BwdWorkspace backward_workspace_layout(const Problem& p);

@@ -57,7 +57,7 @@ extern "C" {
 
 fa_status fa_backward_noalloc(const fa_dims* dims, const void* Q, const void* K, const void* V, const void* O,
                               const void* dO, const float* L, void* dQ, void* dK, void* dV, void* stream) {
-  const size_t need = fa_backward_workspace_bytes(dims);  // 0 for invalid dims: rejected below
+  const size_t need = fa_backward_workspace_min_bytes(dims);  // 0 for invalid dims: rejected below
   if (need > (size_t)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_TOO_SMALL;
   void* scratch = scratch_for_current_device();
   if (!scratch) return FA_ERR_CUDA;
