@@ -36,7 +36,7 @@
  *
  * Supported: d and dv each in {64, 128} (dv may differ from d).  Any B, Hq, Hkv, Tq, Tk >= 0 (ragged tails
  * are handled; a zero-sized problem is a no-op; Tk == 0 yields O = 0 and
- * L = -inf), up to grid limits: Tq <= 65535 * 256, B * Hkv * ceil(Tk / 128)
+ * L = -inf), up to size limits: Tq <= 65535 * 256, B * Hkv * ceil(Tk / 128)
  * < 2^31, B * Hq < 2^31 (beyond them FA_ERR_UNSUPPORTED).
  *
  * Ownership and execution: the caller allocates and frees every buffer,

@@ -58,8 +58,9 @@ fa_status check_dims(const fa_dims* dims, fa::Problem* pr) {
   // TMA coordinates and grid dimensions are 32-bit; keep every index in range.
   if ((long long)z.B * z.Hq > 0x7fffffffLL || (long long)z.B * z.Hkv > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (z.Tq > (1 << 30) || z.Tk > (1 << 30)) return FA_ERR_UNSUPPORTED;
-  // Grid limits: the forward's second grid dimension (pairs of 128-row query
-  // tiles) and the backward's linear grid of (batch, kv head, key tile) CTAs.
+  // Size limits: the forward's pairs of 128-row query tiles per head (kept
+  // within 16 bits, which bounds Tq at 65535 * 256) and the backward's linear
+  // grid of (batch, kv head, key tile) CTAs.
   const long long q_pairs = ((long long)z.Tq + 255) / 256, kv_tiles = ((long long)z.Tk + 127) / 128;
   if (q_pairs > 65535 || (long long)z.B * z.Hkv * kv_tiles > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   pr->B = z.B;
