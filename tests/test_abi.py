@@ -66,7 +66,7 @@ def test_invalid_dims_rejected(bad):
 
 
 @pytest.mark.parametrize("bad", [dict(d=96, dv=96), dict(d=64, dv=96), dict(d=256, dv=256), dict(d=128, dv=32),
-                                 dict(Tq=65535 * 256 + 1),                       # forward grid limit
+                                 dict(Tq=65535 * 256 + 1),                       # Tq size limit
                                  dict(B=1 << 12, Hq=1 << 12, Hkv=1 << 12, Tk=1 << 20)])  # backward grid limit
 def test_unsupported_dims(bad):
     assert call_fwd(dims(**bad)) == fa.FA_ERR_UNSUPPORTED
